@@ -1,0 +1,493 @@
+"""Pins for the fp64 oracle: checks against what the pages and mathematics fix.
+
+None of these re-types an oracle formula.  They use printed values from the
+pages (tests/golden/), closed forms, exhaustive enumeration of a toy model,
+brute-force loops and independent library routines.  The mutation tests at
+the end plant plausible mistakes in the oracle (on the CPU) and show that a
+pin catches each one.
+"""
+import json
+import math
+import os
+from functools import lru_cache
+
+import numpy as np
+import pytest
+import scipy.special
+
+import oracle
+from oracle import spec_oracle as so
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name), encoding="utf-8") as f:
+        return json.load(f)
+
+
+# ---------------------------------------------------------------------------
+# input widening, softmax, argmax
+# ---------------------------------------------------------------------------
+def test_bf16_widening_known_patterns():
+    bits = np.array([0x3F80, 0xC000, 0x3F81, 0x0000, 0x8000, 0x7F7F, 0x0001, 0xFF80],
+                    dtype=np.uint16)
+    want = [1.0, -2.0, 1.0 + 2.0 ** -7, 0.0, -0.0, (2 - 2 ** -7) * 2.0 ** 127,
+            2.0 ** -133, -math.inf]
+    got = so.bf16_bits_to_f64(bits)
+    for g, w in zip(got, want):
+        assert g == w
+
+
+@pytest.mark.parametrize("T", [0.5, 0.7, 1.0, 1.2, 3.0])
+def test_log_normaliser_matches_scipy_logsumexp(T):
+    rng = np.random.default_rng(11)
+    for V in (8, 4096, 262144):
+        x = rng.normal(0, 4, V)
+        L = so.row_log_normaliser(x, T)
+        assert abs(L - scipy.special.logsumexp(x / T)) <= 1e-12 * max(1.0, abs(L))
+        p = so.row_probs(x, T)
+        assert abs(math.fsum(p) - 1.0) < 1e-12
+        # softmax ratio identity: p_a / p_b = exp((x_a - x_b)/T)
+        a, b = 3, 5
+        assert abs(p[a] / p[b] - math.exp((x[a] - x[b]) / T)) < 1e-9 * p[a] / p[b]
+
+
+def test_log_normaliser_with_masked_entries():
+    x = np.array([0.0, -np.inf, math.log(3.0), -np.inf])
+    assert abs(so.row_log_normaliser(x, 1.0) - math.log(4.0)) < 1e-15
+    assert so.row_probs(x, 1.0)[1] == 0.0
+
+
+def test_argmax_lowest_index_on_ties_matches_numpy():
+    rng = np.random.default_rng(5)
+    for _ in range(200):
+        x = rng.integers(-3, 4, size=rng.integers(1, 64)).astype(np.float64)
+        assert so.row_argmax(x) == int(np.argmax(x))  # numpy returns the first max
+
+
+# ---------------------------------------------------------------------------
+# the worked example of the book chapter (golden fixture)
+# ---------------------------------------------------------------------------
+def _one_hot_rows(choices, V, hi=5.0):
+    rows = np.zeros((len(choices), V))
+    for j, c in enumerate(choices):
+        rows[j, c] = hi
+    return rows
+
+
+def worked_example_failures(verify=None):
+    verify = verify or so.verify_greedy_seq
+    g = _golden("book_ch8_worked_example.json")
+    vocab = {t: i for i, t in enumerate(g["vocab"])}
+    tn = g["target_next"]
+    target_next = [vocab[tn[k]] for k in ("row0_after_context", "row1_after_我",
+                                           "row2_after_我们", "row3_after_我们去",
+                                           "row4_after_我们去园")]
+    rows = _one_hot_rows(target_next, len(vocab))
+    bad = 0
+    for case in ("case_mismatch", "case_all_correct"):
+        c = g[case]
+        drafts = [vocab[t] for t in c["drafts"]]
+        res = verify(rows, drafts)
+        want = [vocab[t] for t in c["expected_output"]]
+        ok = (res.n == c["expected_accepted"] and res.tokens[:res.n + 1] == want
+              and all(t == -1 for t in res.tokens[res.n + 1:]))
+        bad += not ok
+    return bad
+
+
+def test_worked_example_book_ch8():
+    assert worked_example_failures() == 0
+
+
+# ---------------------------------------------------------------------------
+# a toy prefix-keyed language model (test-only; not oracle code)
+# ---------------------------------------------------------------------------
+def _toy_logits(prefix, salt, V, sd):
+    ss = np.random.SeedSequence([salt, V, len(prefix), *prefix])
+    return np.random.default_rng(ss).normal(0.0, sd, V)
+
+
+class ToyLM:
+    """p(.|prefix) and q(.|prefix) over V tokens, fixed by hashing the prefix."""
+
+    def __init__(self, V, salt=0, sd=1.5, draft_noise=0.8):
+        self.V, self.salt, self.sd, self.dn = V, salt, sd, draft_noise
+
+    def target_logits(self, prefix):
+        return _toy_logits(tuple(prefix), self.salt, self.V, self.sd)
+
+    def draft_logits(self, prefix):
+        return self.target_logits(prefix) + self.dn * _toy_logits(tuple(prefix), self.salt + 1000, self.V, 1.0)
+
+
+def _greedy_chain(lm, prompt, n):
+    pre, out = list(prompt), []
+    for _ in range(n):
+        t = int(np.argmax(lm.target_logits(pre)))
+        out.append(t)
+        pre.append(t)
+    return out
+
+
+def _spec_greedy(lm, prompt, n, gamma, verify=None):
+    verify = verify or so.verify_greedy_seq
+    pre, out = list(prompt), []
+    while len(out) < n:
+        drafts, cur = [], list(pre)
+        for _ in range(gamma):
+            d = int(np.argmax(lm.draft_logits(cur)))
+            drafts.append(d)
+            cur.append(d)
+        rows = np.stack([lm.target_logits(pre + drafts[:j]) for j in range(gamma + 1)])
+        res = verify(rows, drafts)
+        emitted = res.tokens[:res.n + 1]
+        assert len(emitted) >= 1 and -1 not in emitted
+        out += emitted
+        pre += emitted
+    return out[:n]
+
+
+def greedy_chain_mismatches(verify=None):
+    bad = 0
+    for salt in range(6):
+        for gamma in (1, 2, 4, 7):
+            lm = ToyLM(V=8, salt=salt)
+            bad += _spec_greedy(lm, [salt % 8], 24, gamma, verify) != _greedy_chain(lm, [salt % 8], 24)
+    return bad
+
+
+def test_greedy_speculation_equals_plain_argmax_chain():
+    """Greedy speculative output is bit-identical to the target's own greedy
+    output ("Gemma 4 MTP 深度解析" §2.2; "自投机解码…" §3.1)."""
+    assert greedy_chain_mismatches() == 0
+
+
+# ---------------------------------------------------------------------------
+# exhaustive enumeration: the output marginal equals the target's own
+# autoregressive distribution ("Gemma 4 MTP 深度解析" §2.2; "第 8 章…" 为什么输出不会变)
+# ---------------------------------------------------------------------------
+def _round_distribution(lm, prefix, gamma, T, mod):
+    """Exact distribution of the tokens one verify round emits from ``prefix``.
+    Uses the oracle's acceptance probability and residual weights; the drafts
+    are drawn from q (enumerated)."""
+    V = lm.V
+    P = lambda pre: mod.row_probs(lm.target_logits(pre), T)
+    Q = lambda pre: mod.row_probs(lm.draft_logits(pre), T)
+    dist = {}
+
+    def add(seq, w):
+        if w > 0:
+            dist[seq] = dist.get(seq, 0.0) + w
+
+    def walk(pre, drafts, weight):
+        j = len(drafts)
+        p, = (P(pre + drafts),)
+        if j == gamma:
+            for t in range(V):
+                add(tuple(drafts) + (t,), weight * p[t])
+            return
+        q = Q(pre + drafts)
+        r = mod.residual_weights(p, q)
+        z = r.sum()
+        for d in range(V):
+            if q[d] == 0:
+                continue
+            a = mod.acceptance_probability(p, q, d)
+            if a < 1 and z > 0:
+                for t in range(V):
+                    add(tuple(drafts) + (t,), weight * q[d] * (1 - a) * r[t] / z)
+            walk(pre, drafts + [d], weight * q[d] * a)
+
+    walk(list(prefix), [], 1.0)
+    return dist
+
+
+def lossless_enumeration_error(mod=so, V=8, gamma=2, T=1.0, k=3, salt=3):
+    lm = ToyLM(V=V, salt=salt, sd=1.2, draft_noise=1.0)
+
+    @lru_cache(maxsize=None)
+    def first_k(prefix, kk):
+        out = {}
+        for seq, w in _round_distribution(lm, list(prefix), gamma, T, mod).items():
+            if len(seq) >= kk:
+                out[seq[:kk]] = out.get(seq[:kk], 0.0) + w
+            else:
+                for rest, w2 in first_k(prefix + seq, kk - len(seq)).items():
+                    out[seq + rest] = out.get(seq + rest, 0.0) + w * w2
+        return out
+
+    spec = first_k((1,), k)
+    err = 0.0
+    for t1 in range(V):
+        p1 = scipy.special.softmax(lm.target_logits([1]) / T)[t1]
+        for t2 in range(V):
+            p2 = scipy.special.softmax(lm.target_logits([1, t1]) / T)[t2]
+            for t3 in range(V):
+                p3 = scipy.special.softmax(lm.target_logits([1, t1, t2]) / T)[t3]
+                err = max(err, abs(spec.get((t1, t2, t3), 0.0) - p1 * p2 * p3))
+    return err
+
+
+@pytest.mark.parametrize("T", [1.0, 0.6])
+def test_lossless_marginal_exact_enumeration_V8_gamma2(T):
+    assert lossless_enumeration_error(T=T) < 1e-12
+
+
+# ---------------------------------------------------------------------------
+# expected tokens per round (closed form printed on the pages)
+# ---------------------------------------------------------------------------
+def _two_token_toy(gamma):
+    """V=2: q = (1, 0), p = (0.8, 0.2) at every position: alpha = 0.8 exactly."""
+    tgt = np.tile(np.log([0.8, 0.2]), (gamma + 1, 1))
+    dft = np.tile(np.array([0.0, -np.inf]), (gamma, 1))
+    return tgt, dft
+
+
+def test_closed_form_expected_tokens_printed_value():
+    g = _golden("closed_forms.json")["expected_tokens"]
+    E = oracle.expected_tokens_per_round(g["alpha"], g["gamma"])
+    assert round(E, g["printed_decimals"]) == g["printed_value"]
+    # the closed form equals the term-by-term sum 1 + alpha + ... + alpha^gamma
+    assert abs(E - math.fsum(g["alpha"] ** k for k in range(g["gamma"] + 1))) < 1e-15
+
+
+def test_tokens_per_round_exact_matches_closed_form():
+    """Exact distribution of the emitted count from the oracle's acceptance
+    probability, against (1 - a^(g+1)) / (1 - a)."""
+    for gamma in (1, 4, 8):
+        tgt, dft = _two_token_toy(gamma)
+        T = 1.0
+        acc = [so.acceptance_probability(so.row_probs(tgt[j], T), so.row_probs(dft[j], T), 0)
+               for j in range(gamma)]
+        surv, E = 1.0, 0.0
+        for j in range(gamma):
+            E += surv * (1 - acc[j]) * (j + 1)
+            surv *= acc[j]
+        E += surv * (gamma + 1)
+        assert abs(E - oracle.expected_tokens_per_round(0.8, gamma)) < 1e-12
+
+
+def tokens_per_round_mc(mod=so, rounds=20000, gamma=4, seed=7):
+    tgt, dft = _two_token_toy(gamma)
+    rng = np.random.default_rng(seed)
+    counts = np.empty(rounds)
+    for i in range(rounds):
+        res = mod.verify_sample_seq(tgt, dft, [0] * gamma, 1.0, rng.random(gamma), rng.random())
+        counts[i] = res.n + 1
+        assert res.tokens[res.n] in (0, 1)
+        if res.n < gamma:
+            assert res.tokens[res.n] == 1  # residual of (0.8,0.2) vs (1,0) is token 1
+    return counts
+
+
+def test_tokens_per_round_monte_carlo_uniform_path():
+    """The uniform-consuming path reproduces E = 3.3616 at alpha=0.8, gamma=4."""
+    c = tokens_per_round_mc()
+    E = oracle.expected_tokens_per_round(0.8, 4)
+    se = c.std(ddof=1) / math.sqrt(len(c))
+    assert abs(c.mean() - E) < 4 * se
+
+
+def first_token_chi2(mod=so, V=8, rounds=20000, seed=13):
+    """Empirical law of the first emitted token vs p_0 (chi-square statistic)."""
+    rng = np.random.default_rng(seed)
+    lt = rng.normal(0, 1.5, (2, V))
+    ld = lt[:1] + rng.normal(0, 1.0, (1, V))
+    p0 = so.row_probs(lt[0], 1.0)
+    q0 = so.row_probs(ld[0], 1.0)
+    counts = np.zeros(V)
+    for _ in range(rounds):
+        d = int(rng.choice(V, p=q0))
+        res = mod.verify_sample_seq(lt, ld, [d], 1.0, [rng.random()], rng.random())
+        counts[res.tokens[0]] += 1
+    expct = rounds * p0
+    return float(np.sum((counts - expct) ** 2 / expct))
+
+
+def test_first_token_law_monte_carlo():
+    # chi-square with 7 dof: P(X > 29) ~ 1.4e-4
+    assert first_token_chi2() < 29.0
+
+
+# ---------------------------------------------------------------------------
+# residual identities, inverse CDF, decisions
+# ---------------------------------------------------------------------------
+def test_residual_identities():
+    """P(accept x) = min(p, q) and the residual restores p exactly
+    ("自投机解码…" §3.2)."""
+    rng = np.random.default_rng(3)
+    for V in (2, 8, 1000):
+        p = so.row_probs(rng.normal(0, 2, V), 1.0)
+        q = so.row_probs(rng.normal(0, 2, V), 1.0)
+        w = so.residual_weights(p, q)
+        Z = w.sum()
+        accept_mass = np.minimum(p, q)
+        assert abs(accept_mass.sum() + Z - 1.0) < 1e-13
+        assert np.max(np.abs(accept_mass + Z * (w / Z) - p)) < 1e-15
+        # rejection probability = sum_x q(x) (1 - min(1, p/q)) = Z
+        rej = math.fsum(q[x] * (1 - so.acceptance_probability(p, q, x)) for x in range(V))
+        assert abs(rej - Z) < 1e-13
+
+
+def _icdf_bruteforce(w, u):
+    """Definition written as a loop: the smallest k whose running total exceeds u*Z."""
+    total = math.fsum(w)
+    run = 0.0
+    for k, x in enumerate(w):
+        run += x
+        if run > u * total:
+            return k
+    return max(i for i, x in enumerate(w) if x > 0)
+
+
+def test_inverse_cdf_hand_cases():
+    w = np.array([0.0, 0.25, 0.0, 0.75])
+    assert so.inverse_cdf(w, 0.0)[0] == 1
+    assert so.inverse_cdf(w, 0.2499)[0] == 1
+    assert so.inverse_cdf(w, 0.25)[0] == 3       # C(1) = 0.25 is not > 0.25
+    assert so.inverse_cdf(w, 0.3)[0] == 3
+    assert so.inverse_cdf(w, 0.999999)[0] == 3
+    k, m = so.inverse_cdf(w, 0.3)
+    assert abs(m - 0.05) < 1e-15
+
+
+def test_inverse_cdf_matches_bruteforce():
+    rng = np.random.default_rng(17)
+    for _ in range(300):
+        V = int(rng.integers(1, 40))
+        w = rng.random(V) * (rng.random(V) < 0.7)
+        if w.sum() == 0:
+            w[rng.integers(V)] = 1.0
+        u = float(rng.random())
+        assert so.inverse_cdf(w, u)[0] == _icdf_bruteforce(w, u)
+
+
+def test_accept_decision_is_strict_u_below_ratio():
+    lt = np.log(np.array([[0.3, 0.7], [0.5, 0.5]]))
+    ld = np.log(np.array([[0.6, 0.4]]))
+    rho = 0.3 / 0.6
+    below = so.verify_sample_seq(lt, ld, [0], 1.0, [np.nextafter(rho, 0)], 0.1)
+    at = so.verify_sample_seq(lt, ld, [0], 1.0, [rho], 0.1)
+    assert below.n == 1 and at.n == 0
+    assert at.tokens[0] == 1          # residual max(0, p-q) = (0, 0.3)
+
+
+def test_special_cases():
+    rng = np.random.default_rng(23)
+    V, gamma = 64, 5
+    lt = rng.normal(0, 2, (gamma + 1, V))
+    # draft logits equal to target: rho = 1 -> all accepted, bonus drawn from p_gamma
+    d = [int(x) for x in rng.integers(0, V, gamma)]
+    u = rng.random(gamma) * 0.999
+    res = so.verify_sample_seq(lt, lt[:gamma], d, 0.8, u, 0.37)
+    assert res.n == gamma and res.path == "bonus"
+    assert res.tokens[gamma] == _icdf_bruteforce(so.row_probs(lt[gamma], 0.8), 0.37)
+    # one-hot target (other entries masked) at a != d: rejected, residual is delta_a
+    one_hot = np.full((gamma + 1, V), -np.inf)
+    one_hot[:, 9] = 0.0
+    res = so.verify_sample_seq(one_hot, lt[:gamma], [3] * gamma, 1.0, [0.0] * gamma, 0.5)
+    assert res.n == 0 and res.tokens[0] == 9
+    # greedy: draft = argmax chain -> n = gamma, bonus = argmax of row gamma
+    dg = [int(np.argmax(lt[j])) for j in range(gamma)]
+    res = so.verify_greedy_seq(lt, dg)
+    assert res.n == gamma and res.tokens[gamma] == int(np.argmax(lt[gamma]))
+    # temperature <= 0 in the sampling entry is a greedy sequence
+    res2 = so.verify_sample_seq(lt, lt[:gamma], dg, 0.0, u, 0.5)
+    assert res2.tokens == res.tokens and res2.path == "greedy"
+
+
+# ---------------------------------------------------------------------------
+# the lm_head product against a brute-force loop
+# ---------------------------------------------------------------------------
+def test_lmhead_logits_bruteforce():
+    rng = np.random.default_rng(29)
+    R, V, H = 3, 5, 7
+    h = rng.normal(0, 1, (R, H)).astype(np.float32)
+    W = rng.normal(0, 0.02, (V, H)).astype(np.float32)
+    got = so.lmhead_logits(h, W)
+    for r in range(R):
+        for x in range(V):
+            want = math.fsum(float(h[r, k]) * float(W[x, k]) for k in range(H))
+            assert abs(got[r, x] - want) < 1e-15
+
+
+# ---------------------------------------------------------------------------
+# speed-up model (host-side closed forms printed on the pages)
+# ---------------------------------------------------------------------------
+def test_speedup_closed_forms_printed_values():
+    g = _golden("closed_forms.json")
+    cf = g["cost_factor"]
+    assert abs((1 + cf["gamma"] * cf["c"]) - cf["printed_value"]) < 1e-12
+    s = g["speedup_naive"]
+    for pt in s["points"]:
+        assert round(oracle.speedup_naive(pt["alpha"], s["gamma"], s["c"]), 2) == pt["printed_value"]
+    gain = oracle.speedup_naive(0.9, 4, 0.02) - oracle.speedup_naive(0.8, 4, 0.02)
+    assert round(gain, 1) == s["gain_0p8_to_0p9_printed"]
+    sw = g["speedup_layer_skip_sweep"]
+    lo = [oracle.speedup_layer_skip(sw["alpha_low"], k, sw["c"]) for k in range(1, 11)]
+    assert all(a > b for a, b in zip(lo, lo[1:]))
+    gstar = oracle.best_gamma(sw["alpha_high"], sw["c"])
+    assert sw["best_gamma_range"][0] <= gstar <= sw["best_gamma_range"][1]
+
+
+# ---------------------------------------------------------------------------
+# planted mistakes: each plausible error must fail one of the pins above
+# ---------------------------------------------------------------------------
+def test_mutation_residual_sign_is_caught(monkeypatch):
+    monkeypatch.setattr(so, "residual_weights", lambda p, q: np.maximum(0.0, q - p))
+    assert lossless_enumeration_error() > 1e-3
+
+
+def test_mutation_inverted_ratio_is_caught(monkeypatch):
+    def bad(p, q, d):
+        return 1.0 if p[d] == 0 else min(1.0, float(q[d] / p[d]))
+    monkeypatch.setattr(so, "acceptance_probability", bad)
+    assert lossless_enumeration_error() > 1e-3
+
+
+def test_mutation_dropped_temperature_is_caught(monkeypatch):
+    orig = so.row_probs
+    monkeypatch.setattr(so, "row_probs", lambda x, T: orig(x, 1.0))
+    assert lossless_enumeration_error(T=0.6) > 1e-3
+
+
+def test_mutation_row_offset_is_caught():
+    def shifted(target_rows, draft_tokens):
+        t = np.asarray(target_rows, dtype=np.float64)
+        rolled = np.concatenate([t[1:], t[-1:]])   # verify d_{j+1} against row j+1
+        return so.verify_greedy_seq(rolled, draft_tokens)
+    assert greedy_chain_mismatches(shifted) > 0
+
+
+def test_mutation_no_bonus_is_caught():
+    def no_bonus(target_rows, draft_tokens):
+        r = so.verify_greedy_seq(target_rows, draft_tokens)
+        if r.n == len(draft_tokens):
+            r.tokens[-1] = -1
+            r.n -= 1   # the all-accepted branch emits nothing extra
+        return r
+    assert worked_example_failures(no_bonus) > 0
+
+
+def test_mutation_wrong_uniform_compare_is_caught(monkeypatch):
+    orig = so.verify_sample_seq
+
+    def flipped(tp, tq, d, T, ua, ur):
+        # reflect u about rho = 0.8 (the toy's ratio): accepts iff u > rho
+        return orig(tp, tq, d, T, [1.6 - u for u in ua], ur)
+    monkeypatch.setattr(so, "verify_sample_seq", flipped)
+    # accept iff u > rho instead of u < rho: the mean count moves far from 3.3616
+    c = tokens_per_round_mc(mod=so, rounds=4000)
+    assert abs(c.mean() - oracle.expected_tokens_per_round(0.8, 4)) > 0.2
+
+
+def test_mutation_icdf_off_by_one_is_caught(monkeypatch):
+    orig = so.inverse_cdf
+
+    def shifted(w, u):
+        k, m = orig(w, u)
+        return min(k + 1, len(w) - 1), m
+    monkeypatch.setattr(so, "inverse_cdf", shifted)
+    assert first_token_chi2(mod=so, rounds=5000) > 29.0
