@@ -1,0 +1,431 @@
+#!/usr/bin/env python
+"""Verify rounds/s and logit HBM GB/s of libspecverify on one GB300 (or N replicas).
+
+Workload (one "step" = one verify round of the whole hot path over one batch):
+batched serving verify, B=32 sequences, gamma=4 drafts, V=262,144 vocabulary,
+bf16 target and draft logits (fp32 math), per-sequence T ~ U[0.5, 1.2],
+rejection-sampling mode.  Inputs are synthetic (seeded, see workloads/), made
+on the GPU before timing; a pool of rounds larger than L2 is cycled so every
+step streams its logits from HBM.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the fp64 CPU oracle (the reference implementation of
+this build) on the host cores on a bounded sample of the same workload.
+Multi-GPU runs are independent replicas (the verify step has no exchange).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "verify rounds/s and logit HBM GB/s (fraction of 8 TB/s) at B×(γ+1)×262K vocab"
+WORKLOAD = ("batched serving verify: B=32, gamma=4, V=262144, bf16 target+draft logits, "
+            "per-sequence T~U[0.5,1.2], rejection sampling")
+NOMINAL_HBM_GBS = 8000.0
+B, GAMMA, V = 32, 4, 262144
+POOL = 4  # rounds in the pool: 4 x 151 MB > L2 (126 MB)
+
+
+def counted_bytes(B, gamma, V, esize, n_sampling):
+    """Bytes of p and q the verify must read: every target row, plus the draft
+    rows of sampling sequences."""
+    return B * (gamma + 1) * V * esize + n_sampling * gamma * V * esize
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas)
+# ---------------------------------------------------------------------------
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def dist_init(ws, backend):
+    import torch.distributed as dist
+    if ws > 1 and not dist.is_initialized():
+        dist.init_process_group(backend)
+
+
+def dist_barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def dist_max(ws, x, device):
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, gpu_id: str | None, period_ms: int = 50):
+        self.proc = None
+        self.lines = []
+        cmd = ["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits",
+               f"-lms={period_ms}"]
+        if gpu_id:
+            cmd.append(f"--id={gpu_id}")
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def mark(self):
+        self.t_mark = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self, skip_first=0):
+        rows = []
+        for ln in self.lines[skip_first:]:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def time_loop(fn, n, stream):
+    import torch
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(n):
+        fn(i)
+    e1.record(stream)
+    e1.synchronize()
+    return e0.elapsed_time(e1) / 1e3
+
+
+def run_ours(args):
+    import torch
+
+    import speculative_decoding_verification_54_gb300 as sv
+    import workloads as wl
+    from speculative_decoding_verification_54_gb300 import _build
+
+    ws_n, rank, local = dist_setup()
+    dist_init(ws_n, "nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    _build.build()
+    sv.load()
+    stream = torch.cuda.current_stream()
+
+    pool = [wl.torch_round("batched", r + 1000 * rank, dev) for r in range(POOL)]
+    esize = 2
+    n_samp = [int((p["temperature"] > 0).sum().item()) for p in pool]
+    bytes_round = [counted_bytes(B, GAMMA, V, esize, n) for n in n_samp]
+    bytes_mean = sum(bytes_round) / len(bytes_round)
+    wsp = sv.make_workspace(B, GAMMA, V, device=dev)
+    out = torch.empty((B, GAMMA + 1), dtype=torch.int32, device=dev)
+    num = torch.empty((B,), dtype=torch.int32, device=dev)
+
+    def step(i):
+        p = pool[i % POOL]
+        sv.spec_verify_sample(p["target"], p["draft"], p["draft_tokens"], p["temperature"],
+                              p["u_accept"], p["u_resample"], out, num, wsp, stream=stream)
+
+    def reduce_step(i):
+        p = pool[i % POOL]
+        sv.spec_verify_sample_reduce_only(p["target"], p["draft"], p["draft_tokens"], p["temperature"],
+                                          p["u_accept"], p["u_resample"], out, num, wsp, stream=stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    assert sv.spec_verify_status(wsp) == sv.SPEC_OK
+
+    gpu_id = None
+    try:
+        gpu_id = str(torch.cuda.get_device_properties(dev).uuid)
+        if not gpu_id.startswith("GPU-"):
+            gpu_id = "GPU-" + gpu_id
+    except Exception:
+        gpu_id = None
+    clocks = ClockSampler(gpu_id)
+    time.sleep(1.0)
+    n_before = 0
+    dist_barrier(ws_n)
+    torch.cuda.synchronize()
+    elapsed = time_loop(step, args.steps, stream)
+    torch.cuda.synchronize()
+    dist_barrier(ws_n)
+    clocks.stop()
+    st = sv.spec_verify_status(wsp)
+    if st != sv.SPEC_OK:
+        raise SystemExit(f"device status after timed loop: {sv.error_string(st)}")
+    elapsed_max = dist_max(ws_n, elapsed, dev)
+
+    value = ws_n * args.steps / elapsed_max
+    gbs = value * bytes_mean / 1e9
+
+    # dominant kernel: the row reducer, launched alone with CUDA events on the same stream
+    for i in range(min(args.warmup, 20)):
+        reduce_step(i)
+    nred = max(50, min(args.steps, 5000))
+    red_s = time_loop(reduce_step, nred, stream) / nred
+    peak, peak_kind = load_peaks()
+    achieved = bytes_mean / red_s / 1e9
+    traffic = None
+    tr_path = os.path.join(ROOT, "profiles", "rowstats_traffic.json")
+    if os.path.exists(tr_path):
+        with open(tr_path) as f:
+            tr = json.load(f)
+        if tr.get("kernel_source_sha") == _source_sha():
+            traffic = tr.get("dram_bytes_per_launch")
+
+    # end to end through the C ABI with host buffers: H2D of the round's inputs
+    # from pinned memory, the call, D2H of the emitted tokens
+    hpool = []
+    for p in pool[:2]:
+        hpool.append({k: (v.to("cpu").pin_memory() if torch.is_tensor(v) else v) for k, v in p.items()})
+    dpool = {k: torch.empty_like(v, device=dev) for k, v in pool[0].items() if torch.is_tensor(v)}
+    hout = torch.empty((B, GAMMA + 1), dtype=torch.int32).pin_memory()
+    hnum = torch.empty((B,), dtype=torch.int32).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for k, v in hpool[0].items() if torch.is_tensor(v))
+    d2h = hout.numel() * 4 + hnum.numel() * 4
+
+    def e2e_step(i):
+        hp = hpool[i % 2]
+        for k, t in dpool.items():
+            t.copy_(hp[k], non_blocking=True)
+        sv.spec_verify_sample(dpool["target"], dpool["draft"], dpool["draft_tokens"], dpool["temperature"],
+                              dpool["u_accept"], dpool["u_resample"], out, num, wsp, stream=stream)
+        hout.copy_(out, non_blocking=True)
+        hnum.copy_(num, non_blocking=True)
+
+    for i in range(3):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    ne2e = max(10, min(args.steps, 400))
+    dist_barrier(ws_n)
+    e2e_s = dist_max(ws_n, time_loop(e2e_step, ne2e, stream), dev)
+    e2e_value = ws_n * ne2e / e2e_s
+
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": "rounds/s", "n_gpus": ws_n,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(elapsed_max / args.steps * 1e3, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "B": B, "gamma": GAMMA, "V": V, "logits_dtype": "bf16",
+                   "global_batch": B * ws_n, "parallelism": f"replicas x{ws_n}",
+                   "l2": f"inputs larger than L2: pool of {POOL} rounds x {bytes_mean / 1e6:.1f} MB cycled"},
+        "logit_gbs": round(gbs, 1), "frac_of_8tbs": round(gbs / ws_n / NOMINAL_HBM_GBS, 4),
+        "frac_of_measured_hbm": round(gbs / ws_n / peak, 4),
+        "roofline": {"bound": "hbm", "kernel": "rowstats_kernel<bf16>", "achieved": round(achieved, 1),
+                     "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback 6.8 TB/s",
+                     "traffic": traffic, "bytes_per_launch": bytes_mean,
+                     "avg_launch_us": round(red_s * 1e6, 3),
+                     "timing": f"CUDA events over {nred} back-to-back reduce-only launches on the bench stream"},
+        "e2e": {"value": round(e2e_value, 2), "unit": "rounds/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": ne2e},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clocks.summary(n_before),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(pool[0], budget_s=args.cpu_seconds)
+    if rank == 0 and not args.no_extra:
+        result["other_workloads"] = other_workloads(sv, dev, stream, args)
+    if ws_n > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+
+
+def _source_sha():
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("rowstats.cuh", "common.cuh"):
+        with open(os.path.join(ROOT, "speculative_decoding_verification_54_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def _round_to_host(p):
+    import numpy as np
+    import torch
+
+    def logits(t):
+        if t.dtype == torch.bfloat16:
+            return t.view(torch.int16).cpu().numpy().view(np.uint16)
+        return t.cpu().numpy()
+
+    return dict(target=logits(p["target"]), draft=logits(p["draft"]),
+                draft_tokens=p["draft_tokens"].cpu().numpy(), temperature=p["temperature"].cpu().numpy(),
+                u_accept=p["u_accept"].cpu().numpy(), u_resample=p["u_resample"].cpu().numpy())
+
+
+def cpu_baseline(p, budget_s=12.0):
+    """The fp64 oracle, as it stands, on the host cores: sequences of one round
+    verified one after another until ``budget_s`` seconds have passed."""
+    import oracle
+    h = _round_to_host(p)
+    Bq = h["draft_tokens"].shape[0]
+    n, t0 = 0, time.perf_counter()
+    while True:
+        b = n % Bq
+        oracle.verify_sample_seq(h["target"][b], h["draft"][b], h["draft_tokens"][b], h["temperature"][b],
+                                 h["u_accept"][b], h["u_resample"][b])
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s and n >= 2:
+            break
+    return {"value": round(n / Bq / el, 4), "unit": "rounds/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n} sequences of one B={Bq} round ({n / Bq:.2f} rounds) in {el:.1f} s, numpy fp64, one thread"}
+
+
+def other_workloads(sv, dev, stream, args):
+    """Rounds/s of the other configurations (same timing method, fewer steps)."""
+    import torch
+
+    import workloads as wl
+    res = {}
+    for name, steps, pool_n in (("single", 2000, 16), ("longdraft", 200, 2)):
+        c = wl.CONFIGS[name]
+        pool = [wl.torch_round(name, r, dev) for r in range(pool_n)]
+        b, g, v = c["B"], c["gamma"], c["V"]
+        esize = 2 if c["dtype"] == "bf16" else 4
+        nb = sum(counted_bytes(b, g, v, esize, int((p["temperature"] > 0).sum().item())) for p in pool) / pool_n
+        w = sv.make_workspace(b, g, v, device=dev)
+        o = torch.empty((b, g + 1), dtype=torch.int32, device=dev)
+        n = torch.empty((b,), dtype=torch.int32, device=dev)
+
+        def st(i, pool=pool, w=w, o=o, n=n):
+            p = pool[i % len(pool)]
+            sv.spec_verify_sample(p["target"], p["draft"], p["draft_tokens"], p["temperature"],
+                                  p["u_accept"], p["u_resample"], o, n, w, stream=stream)
+        for i in range(5):
+            st(i)
+        torch.cuda.synchronize()
+        el = time_loop(st, steps, stream)
+        assert sv.spec_verify_status(w) == sv.SPEC_OK
+        rps = steps / el
+        res[name] = {"rounds_per_s": round(rps, 1), "us_per_round": round(el / steps * 1e6, 2),
+                     "logit_gbs": round(rps * nb / 1e9, 1), "frac_of_8tbs": round(rps * nb / 1e9 / NOMINAL_HBM_GBS, 4),
+                     "B": b, "gamma": g, "V": v, "logits_dtype": c["dtype"], "steps": steps}
+        del pool
+        torch.cuda.empty_cache()
+    return res
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the fp64 CPU oracle on the host cores
+# ---------------------------------------------------------------------------
+def run_reference(args):
+    ws_n, rank, _ = dist_setup()
+    if rank != 0:
+        return
+    import numpy as np
+
+    import oracle
+    import workloads as wl
+    inp = wl.make_round("batched", 0)
+    # bound the whole run to about two minutes: one sequence per step when that
+    # fits, else the first V' logits of each row of one sequence (V' >= 4096)
+    est_seq_s = 0.08
+    total = args.steps + args.warmup
+    frac = min(1.0, 120.0 / max(1, total) / est_seq_s)
+    Vs = V if frac >= 1.0 else max(4096, int(V * frac) // 8 * 8)
+    t0 = None
+    for i in range(total):
+        if i == args.warmup:
+            t0 = time.perf_counter()
+        b = i % B
+        oracle.verify_sample_seq(inp.target[b][:, :Vs], inp.draft[b][:, :Vs],
+                                 np.minimum(inp.draft_tokens[b], Vs - 1), inp.temperature[b],
+                                 inp.u_accept[b], inp.u_resample[b])
+    el = time.perf_counter() - t0
+    rounds = args.steps * (Vs / V) / B
+    value = rounds / el
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "rounds/s",
+        "n_gpus": ws_n, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(el / args.steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "B": B, "gamma": GAMMA, "V": V, "logits_dtype": "bf16"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "rounds/s", "cores": 1, "kind": "oracle",
+                         "sample": f"each step verifies one sequence of a B={B} round"
+                                   + ("" if Vs == V else f" over its first {Vs} vocabulary entries")
+                                   + "; value scaled to whole rounds"},
+        "e2e": {"value": round(value, 4), "unit": "rounds/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=None)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.impl == "reference":
+        args.steps = 100 if args.steps is None else args.steps
+        args.warmup = 3 if args.warmup is None else args.warmup
+        run_reference(args)
+    else:
+        args.steps = 20000 if args.steps is None else args.steps
+        args.warmup = 20 if args.warmup is None else max(3, args.warmup)
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,160 @@
+/*
+ * spec_verify.h — C ABI of libspecverify: the verify-and-accept step of
+ * speculative decoding on one NVIDIA GB300 (sm_103a).
+ *
+ * After the target model's single forward pass over the gamma+1 verify
+ * positions of a sequence (prefix + draft tokens d_1..d_gamma), row j of the
+ * target logits is its next-token distribution after prefix + d_1..d_j
+ * ("第 8 章 投机解码：一次前向，验证好几个字", section 为什么一次前向能验证多个 token).
+ * This library turns those logits (and, when sampling, the drafter's logits)
+ * into the tokens the round emits.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Every tensor argument is a DEVICE pointer owned by the caller, row-major
+ *   and contiguous.  Logit tensors must be 16-byte aligned and V must be a
+ *   multiple of 8 (rows are moved as 16-byte vectors by bulk copies).
+ * - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *   All work is enqueued on it; calls return before the GPU finishes.
+ * - The library allocates nothing per call.  Scratch state lives in a
+ *   caller-owned device workspace of spec_verify_workspace_bytes() bytes,
+ *   256-byte aligned, ZEROED ONCE before its first use (cudaMemset or
+ *   spec_verify_workspace_init).  A workspace serves one call at a time; calls
+ *   on different workspaces are independent.
+ * - Host-side argument checks run before anything is enqueued and return a
+ *   negative code.  Errors found on the device (a wait that ran out, a draft
+ *   token outside [0, V)) are recorded in the workspace and reported by
+ *   spec_verify_status().  No C++ exception crosses this boundary.
+ * - Temperatures: T <= 0 (or NaN) marks a greedy sequence.  Logits must be
+ *   finite or -inf; NaN/+inf logits give unspecified tokens.
+ * - out_tokens [B, gamma+1] int32: for sequence b the first n+1 entries are
+ *   the emitted tokens (n accepted drafts, then the replacement / resampled /
+ *   bonus token); the remaining entries are -1.  out_num_accepted [B] = n.
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype;
+
+enum {
+  SPEC_OK = 0,
+  SPEC_ERR_INVALID_ARG = -1,  /* null pointer, B < 1, gamma outside 1..31, V bad */
+  SPEC_ERR_UNSUPPORTED = -2,  /* dtype / shape not supported by this build      */
+  SPEC_ERR_ALIGNMENT = -3,    /* a logit pointer is not 16-byte aligned         */
+  SPEC_ERR_WORKSPACE = -4,    /* workspace null, misaligned or too small        */
+  SPEC_ERR_CUDA = -5,         /* a CUDA runtime call or kernel launch failed    */
+  SPEC_ERR_TIMEOUT = -6,      /* device side: a bounded wait ran out            */
+  SPEC_ERR_DEVICE_INPUT = -7  /* device side: a draft token outside [0, V)      */
+};
+
+#define SPEC_MAX_GAMMA 31
+#define SPEC_MAX_VOCAB (1 << 26)
+
+/*
+ * Bytes of workspace needed for batches up to B sequences, draft length up to
+ * gamma and vocabulary up to V (H = lm_head hidden size, 0 when the lm_head
+ * entry point is not used).  Writes *bytes; returns SPEC_OK or
+ * SPEC_ERR_INVALID_ARG.
+ */
+int spec_verify_workspace_bytes(int B, int gamma, int V, int H, size_t *bytes);
+
+/* Zero a workspace on `stream` (equivalent to cudaMemsetAsync(ws, 0, bytes)). */
+int spec_verify_workspace_init(void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Greedy verification ("Accelerating Gemma 4: faster inference with
+ * multi-token prediction drafters", §3.2 验证与接受机制; "自投机解码：层跳过与拒绝采样
+ * 实现大模型推理加速", §3.1 贪心解码).
+ *
+ *   target_logits [B, gamma+1, V] (dtype dt)   row j scores position j
+ *   draft_tokens  [B, gamma] int32              d_{j+1} is checked against row j
+ *
+ * Draft d_{j+1} is accepted iff it equals the argmax of the raw logits of row
+ * j (lowest index on ties).  At the first mismatch n the target's argmax of
+ * row n replaces the draft and the rest is discarded; when all gamma drafts
+ * match, the argmax of row gamma is emitted as the bonus token ("第 8 章 …",
+ * section 多出来的那一个 token 从哪来).  The draft logits are never read.
+ */
+int spec_verify_greedy(const void *target_logits, spec_dtype dt,
+                       const int32_t *draft_tokens, int B, int gamma, int V,
+                       int32_t *out_tokens, int32_t *out_num_accepted,
+                       void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Rejection-sampling verification ("Gemma 4 Multi-Token Prediction (MTP)
+ * 深度解析", §2.2 推测解码的数学保证; "第 8 章 …", section 为什么输出不会变;
+ * "自投机解码 …", §3.2 采样解码 and §3.3 随机数与 batch 内对齐).
+ *
+ *   target_logits [B, gamma+1, V], draft_logits [B, gamma, V] (both dtype dt)
+ *   draft_tokens  [B, gamma] int32
+ *   temperature   [B] float32; T_b <= 0 makes sequence b greedy (as above)
+ *   u_accept      [B, gamma] float32 in [0, 1): one uniform per draft position
+ *   u_resample    [B] float32 in [0, 1): one uniform per sequence
+ *   out_debug     optional [B, gamma+1, 4] float32 (NULL to skip): for j < gamma
+ *                 {p_j(d_{j+1}), q_j(d_{j+1}), L_p[j], L_q[j]}, for j = gamma
+ *                 {0, 0, L_p[gamma], 0}; L = ln sum exp(l/T).  NaN for greedy.
+ *
+ * With p_j = softmax(l_p[j]/T_b) and q_j = softmax(l_q[j]/T_b), draft d_{j+1}
+ * is accepted iff u_accept[b,j] < p_j(d)/q_j(d) (probability min(1, p/q)).
+ * The first rejection n stops the walk; position n is drawn from
+ * max(0, p_n - q_n)/Z by inverse CDF: the smallest token k with
+ * sum_{x<=k} w(x) > u_resample[b]*Z.  If every draft passes, the bonus token
+ * is drawn from p_gamma the same way.
+ */
+int spec_verify_sample(const void *target_logits, const void *draft_logits,
+                       spec_dtype dt, const int32_t *draft_tokens,
+                       const float *temperature, const float *u_accept,
+                       const float *u_resample, int B, int gamma, int V,
+                       int32_t *out_tokens, int32_t *out_num_accepted,
+                       float *out_debug, void *workspace,
+                       size_t workspace_bytes, void *stream);
+
+/*
+ * Timing / profiling aid: the same arguments and checks as
+ * spec_verify_sample, but only the first kernel of its launch chain (the
+ * vocab-row reducer, which streams every logit the call reads) is enqueued,
+ * in the launch configuration spec_verify_sample uses.  Outputs are not
+ * written.  A later spec_verify_sample call is unaffected.
+ */
+int spec_verify_sample_reduce_only(const void *target_logits, const void *draft_logits,
+                                   spec_dtype dt, const int32_t *draft_tokens,
+                                   const float *temperature, const float *u_accept,
+                                   const float *u_resample, int B, int gamma, int V,
+                                   int32_t *out_tokens, int32_t *out_num_accepted,
+                                   float *out_debug, void *workspace,
+                                   size_t workspace_bytes, void *stream);
+
+/*
+ * Synchronise `stream`, then return the device-side status recorded in
+ * `workspace` since the last call (SPEC_OK, SPEC_ERR_TIMEOUT or
+ * SPEC_ERR_DEVICE_INPUT) and clear it.  Returns SPEC_ERR_CUDA if the
+ * synchronisation itself fails.
+ */
+int spec_verify_status(void *workspace, void *stream);
+
+/*
+ * Self-test of the bounded waits: enqueue one tiny kernel whose only wait can
+ * never be satisfied; it gives up after about a millisecond, records
+ * SPEC_ERR_TIMEOUT in `workspace` and returns, leaving the context usable.
+ * spec_verify_status() then reports SPEC_ERR_TIMEOUT.  No data is read.
+ */
+int spec_verify_selftest_timeout(void *workspace, size_t workspace_bytes, void *stream);
+
+/* Static description of an error code. */
+const char *spec_verify_error_string(int code);
+
+/* Library ABI version (major * 10000 + minor * 100 + patch). */
+int spec_verify_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_VERIFY_H */

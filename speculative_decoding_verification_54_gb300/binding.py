@@ -1,0 +1,196 @@
+"""Thin ctypes binding of libspecverify (spec_verify.h), same names as the C ABI.
+
+Argument marshalling only: every step of the verify path runs in the CUDA
+kernels of the shared library.  Tensors are torch CUDA tensors (PyTorch is
+used for device memory and streams); raw integer device addresses are also
+accepted where noted.  A missing or unloadable library raises immediately —
+there is no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import _build
+
+SPEC_F32, SPEC_BF16 = 0, 1
+SPEC_OK = 0
+SPEC_ERR_INVALID_ARG = -1
+SPEC_ERR_UNSUPPORTED = -2
+SPEC_ERR_ALIGNMENT = -3
+SPEC_ERR_WORKSPACE = -4
+SPEC_ERR_CUDA = -5
+SPEC_ERR_TIMEOUT = -6
+SPEC_ERR_DEVICE_INPUT = -7
+MAX_GAMMA = 31
+
+EXPORTED = (
+    "spec_verify_workspace_bytes", "spec_verify_workspace_init", "spec_verify_greedy",
+    "spec_verify_sample", "spec_verify_status", "spec_verify_error_string",
+    "spec_verify_version", "spec_verify_selftest_timeout", "spec_verify_sample_reduce_only",
+)
+
+
+class SpecVerifyError(RuntimeError):
+    def __init__(self, code: int, what: str = ""):
+        self.code = code
+        super().__init__(f"{what}: {error_string(code)} ({code})" if what else f"{error_string(code)} ({code})")
+
+
+_lib = None
+_vp, _sz, _i = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load the shared library (built by ``__graft_entry__.build()``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or lib_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"libspecverify not built ({path} missing); run __graft_entry__.build()")
+    lib = ctypes.CDLL(path)
+    lib.spec_verify_workspace_bytes.argtypes = [_i, _i, _i, _i, ctypes.POINTER(_sz)]
+    lib.spec_verify_workspace_init.argtypes = [_vp, _sz, _vp]
+    lib.spec_verify_greedy.argtypes = [_vp, _i, _vp, _i, _i, _i, _vp, _vp, _vp, _sz, _vp]
+    lib.spec_verify_sample.argtypes = [_vp, _vp, _i, _vp, _vp, _vp, _vp, _i, _i, _i,
+                                       _vp, _vp, _vp, _vp, _sz, _vp]
+    lib.spec_verify_sample_reduce_only.argtypes = list(lib.spec_verify_sample.argtypes)
+    lib.spec_verify_status.argtypes = [_vp, _vp]
+    lib.spec_verify_error_string.argtypes = [_i]
+    lib.spec_verify_error_string.restype = ctypes.c_char_p
+    lib.spec_verify_version.argtypes = []
+    lib.spec_verify_selftest_timeout.argtypes = [_vp, _sz, _vp]
+    for name in EXPORTED:
+        if name not in ("spec_verify_error_string",):
+            getattr(lib, name).restype = _i
+    _lib = lib
+    return lib
+
+
+def error_string(code: int) -> str:
+    return load().spec_verify_error_string(int(code)).decode()
+
+
+# ---------------------------------------------------------------------------
+# marshalling helpers
+# ---------------------------------------------------------------------------
+def _ptr(t):
+    """Device address of a tensor (or an int address), None for None."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.float32:
+        return SPEC_F32
+    if t.dtype == torch.bfloat16:
+        return SPEC_BF16
+    raise SpecVerifyError(SPEC_ERR_UNSUPPORTED, f"logits dtype {t.dtype}")
+
+
+def _check(code: int, what: str) -> int:
+    if code != SPEC_OK:
+        raise SpecVerifyError(code, what)
+    return code
+
+
+def _nbytes(t) -> int:
+    return t.numel() * t.element_size()
+
+
+# ---------------------------------------------------------------------------
+# the C ABI, one wrapper per entry point
+# ---------------------------------------------------------------------------
+def spec_verify_workspace_bytes(B: int, gamma: int, V: int, H: int = 0) -> int:
+    out = _sz(0)
+    _check(load().spec_verify_workspace_bytes(B, gamma, V, H, ctypes.byref(out)),
+           "spec_verify_workspace_bytes")
+    return out.value
+
+
+def spec_verify_workspace_init(workspace, stream=None) -> None:
+    _check(load().spec_verify_workspace_init(_ptr(workspace), _nbytes(workspace), _stream(stream)),
+           "spec_verify_workspace_init")
+
+
+def make_workspace(B: int, gamma: int, V: int, H: int = 0, device="cuda"):
+    """Allocate (torch) and zero a workspace big enough for (B, gamma, V, H)."""
+    import torch
+    n = spec_verify_workspace_bytes(B, gamma, V, H)
+    ws = torch.zeros(n + 256, dtype=torch.uint8, device=device)
+    off = (-ws.data_ptr()) % 256
+    return ws[off:off + n]
+
+
+def spec_verify_greedy(target_logits, draft_tokens, out_tokens, out_num_accepted, workspace,
+                       stream=None) -> None:
+    """target_logits [B, gamma+1, V] (fp32/bf16), draft_tokens [B, gamma] int32."""
+    B, g1, V = target_logits.shape
+    gamma = g1 - 1
+    _check(load().spec_verify_greedy(_ptr(target_logits), _dtype_code(target_logits),
+                                     _ptr(draft_tokens), B, gamma, V, _ptr(out_tokens),
+                                     _ptr(out_num_accepted), _ptr(workspace), _nbytes(workspace),
+                                     _stream(stream)), "spec_verify_greedy")
+
+
+def spec_verify_sample(target_logits, draft_logits, draft_tokens, temperature, u_accept,
+                       u_resample, out_tokens, out_num_accepted, workspace, out_debug=None,
+                       stream=None) -> None:
+    """target_logits [B, gamma+1, V], draft_logits [B, gamma, V] (same dtype),
+    draft_tokens [B, gamma] int32, temperature [B], u_accept [B, gamma],
+    u_resample [B] (float32); out_tokens [B, gamma+1], out_num_accepted [B]
+    int32; optional out_debug [B, gamma+1, 4] float32."""
+    B, g1, V = target_logits.shape
+    gamma = g1 - 1
+    if draft_logits.dtype != target_logits.dtype:
+        raise SpecVerifyError(SPEC_ERR_UNSUPPORTED, "target and draft logits differ in dtype")
+    _check(load().spec_verify_sample(_ptr(target_logits), _ptr(draft_logits),
+                                     _dtype_code(target_logits), _ptr(draft_tokens),
+                                     _ptr(temperature), _ptr(u_accept), _ptr(u_resample), B, gamma, V,
+                                     _ptr(out_tokens), _ptr(out_num_accepted), _ptr(out_debug),
+                                     _ptr(workspace), _nbytes(workspace), _stream(stream)),
+           "spec_verify_sample")
+
+
+def spec_verify_sample_reduce_only(target_logits, draft_logits, draft_tokens, temperature,
+                                   u_accept, u_resample, out_tokens, out_num_accepted, workspace,
+                                   out_debug=None, stream=None) -> None:
+    """Enqueue only the row-reducer kernel of spec_verify_sample (timing aid)."""
+    B, g1, V = target_logits.shape
+    _check(load().spec_verify_sample_reduce_only(
+        _ptr(target_logits), _ptr(draft_logits), _dtype_code(target_logits), _ptr(draft_tokens),
+        _ptr(temperature), _ptr(u_accept), _ptr(u_resample), B, g1 - 1, V, _ptr(out_tokens),
+        _ptr(out_num_accepted), _ptr(out_debug), _ptr(workspace), _nbytes(workspace),
+        _stream(stream)), "spec_verify_sample_reduce_only")
+
+
+def spec_verify_status(workspace, stream=None) -> int:
+    """Synchronise and return (and clear) the device-side status code."""
+    return load().spec_verify_status(_ptr(workspace), _stream(stream))
+
+
+def spec_verify_version() -> int:
+    return load().spec_verify_version()
+
+
+def spec_verify_selftest_timeout(workspace, stream=None) -> None:
+    _check(load().spec_verify_selftest_timeout(_ptr(workspace), _nbytes(workspace), _stream(stream)),
+           "spec_verify_selftest_timeout")

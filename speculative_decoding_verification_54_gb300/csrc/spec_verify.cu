@@ -1,0 +1,374 @@
+// spec_verify.cu — host side of libspecverify: argument checks, workspace
+// layout and kernel launches behind the C ABI declared in spec_verify.h.
+//
+// Launch chain of one call (all on the caller's stream):
+//   greedy:  rowstats (argmax of target rows)  -> accept
+//   sample:  rowstats (softmax stats of target + draft rows) -> accept
+//            -> residual_mass -> sample
+// Later kernels are launched with programmatic stream serialization so their
+// launch latency overlaps the tail of the previous kernel; each one waits for
+// its predecessor's results with griddepcontrol.wait before reading them.
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "accept.cuh"
+#include "common.cuh"
+#include "rowstats.cuh"
+#include "sample.cuh"
+#include "spec_verify.h"
+
+using namespace specv;
+
+namespace {
+
+constexpr int kMinChunk = 1024;  // smallest vocab chunk (elements)
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  int sms = 0;
+  bool ready = false;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+int device_info(DeviceInfo* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SPEC_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready) {
+    if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return SPEC_ERR_CUDA;
+    const int smem = static_cast<int>(kRingBytes);
+    if (cudaFuncSetAttribute(rowstats_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(rowstats_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem) != cudaSuccess)
+      return SPEC_ERR_CUDA;
+    d.ready = true;
+  }
+  *out = d;
+  return SPEC_OK;
+}
+
+struct Layout {
+  size_t header, partials, rowstat, seq, mass, total;
+};
+
+// Offsets of the workspace regions for a call with (B, gamma, V); sized for
+// the smallest chunk so any chunk choice fits.
+Layout layout(int B, int gamma, int V) {
+  const size_t slots = static_cast<size_t>(B) * (2 * gamma + 1);
+  const size_t cpr = (static_cast<size_t>(V) + kMinChunk - 1) / kMinChunk;
+  Layout L;
+  size_t off = 0;
+  L.header = off;
+  off += align_up(sizeof(WsHeader), 256);
+  L.partials = off;
+  off += align_up(slots * cpr * sizeof(float4), 256);
+  L.rowstat = off;
+  off += align_up(slots * sizeof(RowStat), 256);
+  L.seq = off;
+  off += align_up(static_cast<size_t>(B) * sizeof(SeqState), 256);
+  L.mass = off;
+  off += align_up(static_cast<size_t>(B) * cpr * sizeof(double), 256);
+  L.total = off;
+  return L;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_shape(int B, int gamma, int V) {
+  if (B < 1 || B > 65535) return SPEC_ERR_INVALID_ARG;
+  if (gamma < 1 || gamma > SPEC_MAX_GAMMA) return SPEC_ERR_INVALID_ARG;
+  if (V < 8 || V > SPEC_MAX_VOCAB || (V % 8) != 0) return SPEC_ERR_INVALID_ARG;
+  return SPEC_OK;
+}
+
+// Chunk size: 16 KB of logits per chunk, halved while the grid would have
+// fewer than ~8 chunks per SM (small batches), never below kMinChunk elements.
+struct Plan {
+  int CE, cpr, n_items, nstages;
+  uint32_t stage_bytes;
+  int grid;
+};
+
+Plan make_plan(int B, int gamma, int V, size_t esize, int sms, bool sampling) {
+  Plan p;
+  const int rows = B * (sampling ? (2 * gamma + 1) : (gamma + 1));
+  int CE = static_cast<int>(16384 / esize);
+  while (CE > kMinChunk && static_cast<long long>(rows) * ((V + CE - 1) / CE) < 8LL * sms) CE >>= 1;
+  p.CE = CE;
+  p.cpr = (V + CE - 1) / CE;
+  p.n_items = B * (2 * gamma + 1) * p.cpr;
+  p.stage_bytes = static_cast<uint32_t>(CE * esize);
+  p.nstages = static_cast<int>(kRingBytes / p.stage_bytes);
+  if (p.nstages > kMaxStages) p.nstages = kMaxStages;
+  const int live_items = rows * p.cpr;
+  p.grid = live_items < sms ? live_items : sms;
+  if (p.grid < 1) p.grid = 1;
+  return p;
+}
+
+template <typename Kern, typename Params>
+cudaError_t launch_pdl(Kern k, dim3 grid, dim3 block, size_t smem, cudaStream_t s, const Params& prm) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, prm);
+}
+
+struct Common {
+  const void* target;
+  const void* draft;
+  spec_dtype dt;
+  const int32_t* draft_tokens;
+  const float* temperature;
+  const float* u_accept;
+  const float* u_resample;
+  int B, gamma, V;
+  int32_t* out_tokens;
+  int32_t* out_num;
+  float* out_debug;
+  void* ws;
+  size_t ws_bytes;
+  cudaStream_t stream;
+  int debug;
+  bool reduce_only;  // launch only the row reducer (timing / profiling)
+};
+
+template <typename T>
+int run_chain(const Common& a, bool sampling) {
+  const Layout L = layout(a.B, a.gamma, a.V);
+  if (a.ws_bytes < L.total) return SPEC_ERR_WORKSPACE;
+  DeviceInfo dev;
+  if (device_info(&dev) != SPEC_OK) return SPEC_ERR_CUDA;
+  uint8_t* ws = static_cast<uint8_t*>(a.ws);
+  int* status = reinterpret_cast<int*>(ws + L.header);
+  const Plan pl = make_plan(a.B, a.gamma, a.V, sizeof(T), dev.sms, sampling);
+
+  RowStatsParams rp;
+  rp.target = a.target;
+  rp.draft = sampling ? a.draft : nullptr;
+  rp.temperature = sampling ? a.temperature : nullptr;
+  rp.partials = reinterpret_cast<float4*>(ws + L.partials);
+  rp.status = status;
+  rp.B = a.B;
+  rp.gamma = a.gamma;
+  rp.V = a.V;
+  rp.CE = pl.CE;
+  rp.cpr = pl.cpr;
+  rp.n_items = pl.n_items;
+  rp.nstages = pl.nstages;
+  rp.stage_bytes = pl.stage_bytes;
+  rp.debug = a.debug;
+  rowstats_kernel<T><<<pl.grid, kRowThreads, kRingBytes, a.stream>>>(rp);
+  if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
+  if (a.debug || a.reduce_only) return SPEC_OK;
+
+  AcceptParams ap;
+  ap.target = a.target;
+  ap.draft = a.draft;
+  ap.draft_tokens = a.draft_tokens;
+  ap.temperature = sampling ? a.temperature : nullptr;
+  ap.u_accept = a.u_accept;
+  ap.partials = rp.partials;
+  ap.rowstat = reinterpret_cast<RowStat*>(ws + L.rowstat);
+  ap.seq = reinterpret_cast<SeqState*>(ws + L.seq);
+  ap.mass = reinterpret_cast<double*>(ws + L.mass);
+  ap.out_tokens = a.out_tokens;
+  ap.out_num = a.out_num;
+  ap.out_debug = sampling ? a.out_debug : nullptr;
+  ap.status = status;
+  ap.B = a.B;
+  ap.gamma = a.gamma;
+  ap.V = a.V;
+  ap.CE = pl.CE;
+  ap.cpr = pl.cpr;
+  if (launch_pdl(accept_kernel<T>, dim3(a.B), dim3(kAcceptThreads), 0, a.stream, ap) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+  if (!sampling) return SPEC_OK;
+
+  SampleParams sp;
+  sp.target = a.target;
+  sp.draft = a.draft;
+  sp.u_resample = a.u_resample;
+  sp.partials = rp.partials;
+  sp.rowstat = ap.rowstat;
+  sp.seq = ap.seq;
+  sp.mass = ap.mass;
+  sp.out_tokens = a.out_tokens;
+  sp.B = a.B;
+  sp.gamma = a.gamma;
+  sp.V = a.V;
+  sp.CE = pl.CE;
+  sp.cpr = pl.cpr;
+  if (launch_pdl(residual_mass_kernel<T>, dim3(pl.cpr, a.B), dim3(kSampleThreads), 0, a.stream, sp) !=
+      cudaSuccess)
+    return SPEC_ERR_CUDA;
+  if (launch_pdl(sample_kernel<T>, dim3(a.B), dim3(kSampleThreads), 0, a.stream, sp) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+  return SPEC_OK;
+}
+
+int dispatch(const Common& a, bool sampling) {
+  if (a.dt == SPEC_F32) return run_chain<float>(a, sampling);
+  if (a.dt == SPEC_BF16) return run_chain<__nv_bfloat16>(a, sampling);
+  return SPEC_ERR_UNSUPPORTED;
+}
+
+}  // namespace
+
+extern "C" {
+
+int spec_verify_version(void) { return 100; }
+
+const char* spec_verify_error_string(int code) {
+  switch (code) {
+    case SPEC_OK: return "ok";
+    case SPEC_ERR_INVALID_ARG: return "invalid argument";
+    case SPEC_ERR_UNSUPPORTED: return "unsupported dtype or shape";
+    case SPEC_ERR_ALIGNMENT: return "logit pointer not 16-byte aligned";
+    case SPEC_ERR_WORKSPACE: return "workspace null, misaligned or too small";
+    case SPEC_ERR_CUDA: return "CUDA runtime error";
+    case SPEC_ERR_TIMEOUT: return "device wait timed out";
+    case SPEC_ERR_DEVICE_INPUT: return "draft token outside [0, V)";
+    default: return "unknown error";
+  }
+}
+
+int spec_verify_workspace_bytes(int B, int gamma, int V, int H, size_t* bytes) {
+  if (bytes == nullptr) return SPEC_ERR_INVALID_ARG;
+  if (check_shape(B, gamma, V) != SPEC_OK || H < 0) return SPEC_ERR_INVALID_ARG;
+  *bytes = layout(B, gamma, V).total;
+  return SPEC_OK;
+}
+
+int spec_verify_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {
+  if (workspace == nullptr) return SPEC_ERR_WORKSPACE;
+  if (cudaMemsetAsync(workspace, 0, workspace_bytes, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+  return SPEC_OK;
+}
+
+int spec_verify_greedy(const void* target_logits, spec_dtype dt, const int32_t* draft_tokens, int B,
+                       int gamma, int V, int32_t* out_tokens, int32_t* out_num_accepted, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  if (target_logits == nullptr || draft_tokens == nullptr || out_tokens == nullptr ||
+      out_num_accepted == nullptr)
+    return SPEC_ERR_INVALID_ARG;
+  if (int e = check_shape(B, gamma, V)) return e;
+  if (dt != SPEC_F32 && dt != SPEC_BF16) return SPEC_ERR_UNSUPPORTED;
+  if (!aligned16(target_logits)) return SPEC_ERR_ALIGNMENT;
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return SPEC_ERR_WORKSPACE;
+  Common a = {};
+  a.target = target_logits;
+  a.dt = dt;
+  a.draft_tokens = draft_tokens;
+  a.B = B;
+  a.gamma = gamma;
+  a.V = V;
+  a.out_tokens = out_tokens;
+  a.out_num = out_num_accepted;
+  a.ws = workspace;
+  a.ws_bytes = workspace_bytes;
+  a.stream = static_cast<cudaStream_t>(stream);
+  return dispatch(a, false);
+}
+
+static int sample_entry(bool reduce_only, const void* target_logits, const void* draft_logits, spec_dtype dt,
+                       const int32_t* draft_tokens, const float* temperature, const float* u_accept,
+                       const float* u_resample, int B, int gamma, int V, int32_t* out_tokens,
+                       int32_t* out_num_accepted, float* out_debug, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  if (target_logits == nullptr || draft_logits == nullptr || draft_tokens == nullptr ||
+      temperature == nullptr || u_accept == nullptr || u_resample == nullptr || out_tokens == nullptr ||
+      out_num_accepted == nullptr)
+    return SPEC_ERR_INVALID_ARG;
+  if (int e = check_shape(B, gamma, V)) return e;
+  if (dt != SPEC_F32 && dt != SPEC_BF16) return SPEC_ERR_UNSUPPORTED;
+  if (!aligned16(target_logits) || !aligned16(draft_logits)) return SPEC_ERR_ALIGNMENT;
+  if (out_debug != nullptr && !aligned16(out_debug)) return SPEC_ERR_ALIGNMENT;
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return SPEC_ERR_WORKSPACE;
+  Common a = {};
+  a.target = target_logits;
+  a.draft = draft_logits;
+  a.dt = dt;
+  a.draft_tokens = draft_tokens;
+  a.temperature = temperature;
+  a.u_accept = u_accept;
+  a.u_resample = u_resample;
+  a.B = B;
+  a.gamma = gamma;
+  a.V = V;
+  a.out_tokens = out_tokens;
+  a.out_num = out_num_accepted;
+  a.out_debug = out_debug;
+  a.ws = workspace;
+  a.ws_bytes = workspace_bytes;
+  a.stream = static_cast<cudaStream_t>(stream);
+  a.reduce_only = reduce_only;
+  return dispatch(a, true);
+}
+
+int spec_verify_sample(const void* target_logits, const void* draft_logits, spec_dtype dt,
+                       const int32_t* draft_tokens, const float* temperature, const float* u_accept,
+                       const float* u_resample, int B, int gamma, int V, int32_t* out_tokens,
+                       int32_t* out_num_accepted, float* out_debug, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  return sample_entry(false, target_logits, draft_logits, dt, draft_tokens, temperature, u_accept,
+                      u_resample, B, gamma, V, out_tokens, out_num_accepted, out_debug, workspace,
+                      workspace_bytes, stream);
+}
+
+int spec_verify_sample_reduce_only(const void* target_logits, const void* draft_logits, spec_dtype dt,
+                                   const int32_t* draft_tokens, const float* temperature,
+                                   const float* u_accept, const float* u_resample, int B, int gamma,
+                                   int V, int32_t* out_tokens, int32_t* out_num_accepted,
+                                   float* out_debug, void* workspace, size_t workspace_bytes,
+                                   void* stream) {
+  return sample_entry(true, target_logits, draft_logits, dt, draft_tokens, temperature, u_accept,
+                      u_resample, B, gamma, V, out_tokens, out_num_accepted, out_debug, workspace,
+                      workspace_bytes, stream);
+}
+
+int spec_verify_status(void* workspace, void* stream) {
+  if (workspace == nullptr) return SPEC_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return SPEC_ERR_CUDA;
+  int st = 0;
+  if (cudaMemcpy(&st, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return SPEC_ERR_CUDA;
+  if (st != 0 && cudaMemset(workspace, 0, sizeof(int)) != cudaSuccess) return SPEC_ERR_CUDA;
+  if (st & kStatusTimeout) return SPEC_ERR_TIMEOUT;
+  if (st & kStatusBadToken) return SPEC_ERR_DEVICE_INPUT;
+  return SPEC_OK;
+}
+
+int spec_verify_selftest_timeout(void* workspace, size_t workspace_bytes, void* stream) {
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return SPEC_ERR_WORKSPACE;
+  if (workspace_bytes < layout(1, 1, 8).total) return SPEC_ERR_WORKSPACE;
+  // one tiny launch whose only wait can never be satisfied (~1 ms limit)
+  Common a = {};
+  a.B = 1;
+  a.gamma = 1;
+  a.V = 8;
+  a.ws = workspace;
+  a.ws_bytes = workspace_bytes;
+  a.stream = static_cast<cudaStream_t>(stream);
+  a.debug = 1;
+  a.target = workspace;  // never read in this mode
+  return run_chain<float>(a, false);
+}
+
+}  // extern "C"

@@ -1,0 +1,129 @@
+"""C-ABI library: loads, exports every symbol spec_verify.h declares, and
+rejects bad arguments on the host before any CUDA call (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import speculative_decoding_verification_54_gb300 as sv
+from speculative_decoding_verification_54_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "spec_verify.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return sv.load()
+
+
+def declared_functions():
+    text = open(HEADER, encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(spec_verify_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_public_entry_points():
+    names = declared_functions()
+    for must in ("spec_verify_greedy", "spec_verify_sample", "spec_verify_workspace_bytes",
+                 "spec_verify_status"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert isinstance(getattr(lib, name), ctypes._CFuncPtr)
+    assert set(declared_functions()) <= set(sv.EXPORTED) | {"spec_verify_error_string"}
+
+
+def test_version_and_error_strings(lib):
+    assert sv.spec_verify_version() >= 100
+    assert sv.error_string(sv.SPEC_OK) == "ok"
+    assert "timed out" in sv.error_string(sv.SPEC_ERR_TIMEOUT)
+    assert sv.error_string(12345) == "unknown error"
+
+
+def test_workspace_bytes(lib):
+    a = sv.spec_verify_workspace_bytes(32, 4, 262144)
+    b = sv.spec_verify_workspace_bytes(64, 4, 262144)
+    c = sv.spec_verify_workspace_bytes(32, 8, 262144)
+    assert 0 < a < b and a < c and a % 256 == 0
+    for bad in ((0, 4, 4096), (8, 0, 4096), (8, 32, 4096), (8, 4, 4100), (8, 4, 0)):
+        with pytest.raises(sv.SpecVerifyError) as e:
+            sv.spec_verify_workspace_bytes(*bad)
+        assert e.value.code == sv.SPEC_ERR_INVALID_ARG
+
+
+# Fake device addresses: validation must reject these without touching them.
+A16, A8, WS = 0x10000, 0x10008, 0x20000
+
+
+def _sample(lib, **kw):
+    args = dict(t=A16, d=A16, dt=sv.SPEC_BF16, tok=A16, temp=A16, ua=A16, ur=A16, B=4, g=4,
+                V=4096, out=A16, num=A16, dbg=None, ws=WS, wsb=1 << 30)
+    args.update(kw)
+    return lib.spec_verify_sample(args["t"], args["d"], args["dt"], args["tok"], args["temp"],
+                                  args["ua"], args["ur"], args["B"], args["g"], args["V"],
+                                  args["out"], args["num"], args["dbg"], args["ws"], args["wsb"],
+                                  None)
+
+
+def _greedy(lib, **kw):
+    args = dict(t=A16, dt=sv.SPEC_F32, tok=A16, B=4, g=4, V=4096, out=A16, num=A16, ws=WS,
+                wsb=1 << 30)
+    args.update(kw)
+    return lib.spec_verify_greedy(args["t"], args["dt"], args["tok"], args["B"], args["g"],
+                                  args["V"], args["out"], args["num"], args["ws"], args["wsb"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(t=None), sv.SPEC_ERR_INVALID_ARG),
+    (dict(d=None), sv.SPEC_ERR_INVALID_ARG),
+    (dict(tok=None), sv.SPEC_ERR_INVALID_ARG),
+    (dict(temp=None), sv.SPEC_ERR_INVALID_ARG),
+    (dict(ua=None), sv.SPEC_ERR_INVALID_ARG),
+    (dict(ur=None), sv.SPEC_ERR_INVALID_ARG),
+    (dict(out=None), sv.SPEC_ERR_INVALID_ARG),
+    (dict(num=None), sv.SPEC_ERR_INVALID_ARG),
+    (dict(B=0), sv.SPEC_ERR_INVALID_ARG),
+    (dict(g=0), sv.SPEC_ERR_INVALID_ARG),
+    (dict(g=32), sv.SPEC_ERR_INVALID_ARG),
+    (dict(V=4100), sv.SPEC_ERR_INVALID_ARG),
+    (dict(V=0), sv.SPEC_ERR_INVALID_ARG),
+    (dict(dt=7), sv.SPEC_ERR_UNSUPPORTED),
+    (dict(t=A8), sv.SPEC_ERR_ALIGNMENT),
+    (dict(d=A8), sv.SPEC_ERR_ALIGNMENT),
+    (dict(dbg=A8), sv.SPEC_ERR_ALIGNMENT),
+    (dict(ws=None), sv.SPEC_ERR_WORKSPACE),
+    (dict(ws=WS + 16), sv.SPEC_ERR_WORKSPACE),
+    (dict(wsb=1024), sv.SPEC_ERR_WORKSPACE),
+])
+def test_sample_rejects_bad_arguments_on_host(lib, kw, code):
+    assert _sample(lib, **kw) == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(t=None), sv.SPEC_ERR_INVALID_ARG),
+    (dict(tok=None), sv.SPEC_ERR_INVALID_ARG),
+    (dict(g=40), sv.SPEC_ERR_INVALID_ARG),
+    (dict(V=12), sv.SPEC_ERR_INVALID_ARG),
+    (dict(dt=-1), sv.SPEC_ERR_UNSUPPORTED),
+    (dict(t=A8), sv.SPEC_ERR_ALIGNMENT),
+    (dict(wsb=10), sv.SPEC_ERR_WORKSPACE),
+])
+def test_greedy_rejects_bad_arguments_on_host(lib, kw, code):
+    assert _greedy(lib, **kw) == code
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    from speculative_decoding_verification_54_gb300 import binding
+    saved = binding._lib
+    binding._lib = None
+    try:
+        with pytest.raises(RuntimeError):
+            binding.load(str(tmp_path / "missing.so"))
+    finally:
+        binding._lib = saved
