@@ -140,6 +140,7 @@ def load_peaks():
 
 
 def time_loop(fn, n, stream):
+    """Seconds for n eager calls fn(0..n-1), CUDA events on ``stream``."""
     import torch
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
@@ -148,6 +149,41 @@ def time_loop(fn, n, stream):
     e1.record(stream)
     e1.synchronize()
     return e0.elapsed_time(e1) / 1e3
+
+
+GRAPH_CHUNK = 100
+
+
+class GraphLoop:
+    """fn(i) for i in 0..n-1 captured into CUDA graphs of up to GRAPH_CHUNK
+    steps each, so the host launch rate does not limit the measurement.
+    Replayed on ``stream``; timed with CUDA events on that stream."""
+
+    def __init__(self, fn, n, stream):
+        import torch
+        self.graphs = []
+        self.stream = stream
+        done = 0
+        with torch.cuda.stream(stream):
+            while done < n:
+                k = min(GRAPH_CHUNK, n - done)
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    for i in range(done, done + k):
+                        fn(i)
+                self.graphs.append(g)
+                done += k
+
+    def run(self):
+        import torch
+        with torch.cuda.stream(self.stream):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(self.stream)
+            for g in self.graphs:
+                g.replay()
+            e1.record(self.stream)
+        e1.synchronize()
+        return e0.elapsed_time(e1) / 1e3
 
 
 def run_ours(args):
@@ -163,7 +199,7 @@ def run_ours(args):
     torch.cuda.set_device(dev)
     _build.build()
     sv.load()
-    stream = torch.cuda.current_stream()
+    stream = torch.cuda.Stream(device=dev)
 
     pool = [wl.torch_round("batched", r + 1000 * rank, dev) for r in range(POOL)]
     esize = 2
@@ -177,17 +213,22 @@ def run_ours(args):
     def step(i):
         p = pool[i % POOL]
         sv.spec_verify_sample(p["target"], p["draft"], p["draft_tokens"], p["temperature"],
-                              p["u_accept"], p["u_resample"], out, num, wsp, stream=stream)
+                              p["u_accept"], p["u_resample"], out, num, wsp)
 
     def reduce_step(i):
         p = pool[i % POOL]
         sv.spec_verify_sample_reduce_only(p["target"], p["draft"], p["draft_tokens"], p["temperature"],
-                                          p["u_accept"], p["u_resample"], out, num, wsp, stream=stream)
+                                          p["u_accept"], p["u_resample"], out, num, wsp)
 
-    for i in range(args.warmup):
-        step(i)
     torch.cuda.synchronize()
-    assert sv.spec_verify_status(wsp) == sv.SPEC_OK
+    with torch.cuda.stream(stream):
+        step(0)  # first call outside capture (per-device set-up)
+    torch.cuda.synchronize()
+    timed = GraphLoop(step, args.steps, stream)
+    warm = GraphLoop(step, args.warmup, stream)
+    warm.run()
+    torch.cuda.synchronize()
+    assert sv.spec_verify_status(wsp, stream) == sv.SPEC_OK
 
     gpu_id = None
     try:
@@ -201,11 +242,11 @@ def run_ours(args):
     n_before = 0
     dist_barrier(ws_n)
     torch.cuda.synchronize()
-    elapsed = time_loop(step, args.steps, stream)
+    elapsed = timed.run()
     torch.cuda.synchronize()
     dist_barrier(ws_n)
     clocks.stop()
-    st = sv.spec_verify_status(wsp)
+    st = sv.spec_verify_status(wsp, stream)
     if st != sv.SPEC_OK:
         raise SystemExit(f"device status after timed loop: {sv.error_string(st)}")
     elapsed_max = dist_max(ws_n, elapsed, dev)
@@ -214,10 +255,11 @@ def run_ours(args):
     gbs = value * bytes_mean / 1e9
 
     # dominant kernel: the row reducer, launched alone with CUDA events on the same stream
-    for i in range(min(args.warmup, 20)):
-        reduce_step(i)
     nred = max(50, min(args.steps, 5000))
-    red_s = time_loop(reduce_step, nred, stream) / nred
+    red_loop = GraphLoop(reduce_step, nred, stream)
+    red_loop.run()
+    red_s = red_loop.run() / nred
+    del red_loop
     peak, peak_kind = load_peaks()
     achieved = bytes_mean / red_s / 1e9
     traffic = None
@@ -228,33 +270,7 @@ def run_ours(args):
         if tr.get("kernel_source_sha") == _source_sha():
             traffic = tr.get("dram_bytes_per_launch")
 
-    # end to end through the C ABI with host buffers: H2D of the round's inputs
-    # from pinned memory, the call, D2H of the emitted tokens
-    hpool = []
-    for p in pool[:2]:
-        hpool.append({k: (v.to("cpu").pin_memory() if torch.is_tensor(v) else v) for k, v in p.items()})
-    dpool = {k: torch.empty_like(v, device=dev) for k, v in pool[0].items() if torch.is_tensor(v)}
-    hout = torch.empty((B, GAMMA + 1), dtype=torch.int32).pin_memory()
-    hnum = torch.empty((B,), dtype=torch.int32).pin_memory()
-    h2d = sum(v.numel() * v.element_size() for k, v in hpool[0].items() if torch.is_tensor(v))
-    d2h = hout.numel() * 4 + hnum.numel() * 4
-
-    def e2e_step(i):
-        hp = hpool[i % 2]
-        for k, t in dpool.items():
-            t.copy_(hp[k], non_blocking=True)
-        sv.spec_verify_sample(dpool["target"], dpool["draft"], dpool["draft_tokens"], dpool["temperature"],
-                              dpool["u_accept"], dpool["u_resample"], out, num, wsp, stream=stream)
-        hout.copy_(out, non_blocking=True)
-        hnum.copy_(num, non_blocking=True)
-
-    for i in range(3):
-        e2e_step(i)
-    torch.cuda.synchronize()
-    ne2e = max(10, min(args.steps, 400))
-    dist_barrier(ws_n)
-    e2e_s = dist_max(ws_n, time_loop(e2e_step, ne2e, stream), dev)
-    e2e_value = ws_n * ne2e / e2e_s
+    e2e = None if args.no_e2e else e2e_leg(sv, pool, out, num, wsp, dev, stream, args, ws_n)
 
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": "rounds/s", "n_gpus": ws_n,
@@ -272,9 +288,9 @@ def run_ours(args):
                      "traffic": traffic, "bytes_per_launch": bytes_mean,
                      "avg_launch_us": round(red_s * 1e6, 3),
                      "timing": f"CUDA events over {nred} back-to-back reduce-only launches on the bench stream"},
-        "e2e": {"value": round(e2e_value, 2), "unit": "rounds/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "steps": ne2e},
+        "e2e": e2e,
         "gpu_launches": 4 * args.steps,
+        "launch": f"CUDA graphs of up to {GRAPH_CHUNK} steps (4 kernels per step), replayed on one stream",
         "clocks": clocks.summary(n_before),
     }
     if rank == 0 and not args.no_cpu_baseline:
@@ -286,6 +302,43 @@ def run_ours(args):
         dist.destroy_process_group()
     if rank == 0:
         print(json.dumps(result), flush=True)
+
+
+def e2e_leg(sv, pool, out, num, wsp, dev, stream, args, ws_n):
+    """End to end through the C ABI with host buffers: every step copies the
+    round's inputs from pinned host memory, calls spec_verify_sample and reads
+    the emitted tokens back."""
+    import torch
+    hpool = []
+    for p in pool[:2]:
+        hpool.append({k: (v.to("cpu").pin_memory() if torch.is_tensor(v) else v) for k, v in p.items()})
+    dpool = {k: torch.empty_like(v, device=dev) for k, v in pool[0].items() if torch.is_tensor(v)}
+    hout = torch.empty(tuple(out.shape), dtype=torch.int32).pin_memory()
+    hnum = torch.empty(tuple(num.shape), dtype=torch.int32).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for k, v in hpool[0].items() if torch.is_tensor(v))
+    d2h = hout.numel() * 4 + hnum.numel() * 4
+
+    def e2e_step(i):
+        hp = hpool[i % 2]
+        for k, t in dpool.items():
+            t.copy_(hp[k], non_blocking=True)
+        sv.spec_verify_sample(dpool["target"], dpool["draft"], dpool["draft_tokens"], dpool["temperature"],
+                              dpool["u_accept"], dpool["u_resample"], out, num, wsp)
+        hout.copy_(out, non_blocking=True)
+        hnum.copy_(num, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            e2e_step(i)
+    torch.cuda.synchronize()
+    ne2e = max(10, min(args.steps, 400))
+    dist_barrier(ws_n)
+    with torch.cuda.stream(stream):
+        el = time_loop(e2e_step, ne2e, stream)
+    el = dist_max(ws_n, el, dev)
+    return {"value": round(ws_n * ne2e / el, 2), "unit": "rounds/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": ne2e,
+            "how": "eager calls; per step 6 pinned-host->device copies, the C-ABI call, 2 device->host copies"}
 
 
 def _source_sha():
@@ -349,12 +402,15 @@ def other_workloads(sv, dev, stream, args):
         def st(i, pool=pool, w=w, o=o, n=n):
             p = pool[i % len(pool)]
             sv.spec_verify_sample(p["target"], p["draft"], p["draft_tokens"], p["temperature"],
-                                  p["u_accept"], p["u_resample"], o, n, w, stream=stream)
-        for i in range(5):
-            st(i)
+                                  p["u_accept"], p["u_resample"], o, n, w)
+        with torch.cuda.stream(stream):
+            st(0)
         torch.cuda.synchronize()
-        el = time_loop(st, steps, stream)
-        assert sv.spec_verify_status(w) == sv.SPEC_OK
+        loop = GraphLoop(st, steps, stream)
+        loop.run()
+        el = loop.run()
+        del loop
+        assert sv.spec_verify_status(w, stream) == sv.SPEC_OK
         rps = steps / el
         res[name] = {"rounds_per_s": round(rps, 1), "us_per_round": round(el / steps * 1e6, 2),
                      "logit_gbs": round(rps * nb / 1e9, 1), "frac_of_8tbs": round(rps * nb / 1e9 / NOMINAL_HBM_GBS, 4),
@@ -416,6 +472,7 @@ def main():
     ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end host-buffer leg")
     args = ap.parse_args()
     if args.impl == "reference":
         args.steps = 100 if args.steps is None else args.steps
