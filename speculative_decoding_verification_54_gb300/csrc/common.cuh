@@ -37,10 +37,11 @@ struct WsHeader {
   int pad[63];
 };
 
-struct RowStat {   // combined statistics of one logits row
-  float mk;        // fl(max_raw * ks): scaled max
-  int argmax;      // lowest index of the raw maximum
-  double lse2;     // log2 of sum_x 2^(fma(x, ks, -mk))
+struct RowStat {  // combined statistics of one logits row
+  float mk;       // fl(max_raw * ks): scaled max
+  int argmax;     // lowest index of the raw maximum (greedy rows)
+  float lse2;     // log2 of sum_x 2^(fma(x, ks, -mk))
+  int pad;
 };
 
 struct SeqState {
@@ -170,6 +171,14 @@ __device__ __forceinline__ bool seq_is_greedy(const float* temperature, int b) {
   if (temperature == nullptr) return true;
   const float t = temperature[b];
   return !(t > 0.0f);
+}
+
+// Compensated (Neumaier) summation: s + c carries the sum to about twice the
+// working precision, so fp32 suffices where fp64 would be slow on GB300.
+__device__ __forceinline__ void neumaier_add(float& s, float& c, float x) {
+  const float t = s + x;
+  c += (fabsf(s) >= fabsf(x)) ? ((s - t) + x) : ((x - t) + s);
+  s = t;
 }
 
 // Merge two online-softmax partials (raw max m, scaled max mk, sum s relative

@@ -72,7 +72,7 @@ Layout layout(int B, int gamma, int V) {
   L.seq = off;
   off += align_up(static_cast<size_t>(B) * sizeof(SeqState), 256);
   L.mass = off;
-  off += align_up(static_cast<size_t>(B) * cpr * sizeof(double), 256);
+  off += align_up(static_cast<size_t>(B) * cpr * sizeof(float), 256);
   L.total = off;
   return L;
 }
@@ -86,7 +86,7 @@ int check_shape(int B, int gamma, int V) {
   return SPEC_OK;
 }
 
-// Chunk size: 16 KB of logits per chunk, halved while the grid would have
+// Chunk size: 4 KB of logits per chunk (one ring stage), halved while the grid would have
 // fewer than ~8 chunks per SM (small batches), never below kMinChunk elements.
 struct Plan {
   int CE, cpr, n_items, nstages;
@@ -97,14 +97,17 @@ struct Plan {
 Plan make_plan(int B, int gamma, int V, size_t esize, int sms, bool sampling) {
   Plan p;
   const int rows = B * (sampling ? (2 * gamma + 1) : (gamma + 1));
-  int CE = static_cast<int>(16384 / esize);
+  int CE = static_cast<int>(kStageBytesMax / esize);
   while (CE > kMinChunk && static_cast<long long>(rows) * ((V + CE - 1) / CE) < 8LL * sms) CE >>= 1;
   p.CE = CE;
   p.cpr = (V + CE - 1) / CE;
   p.n_items = B * (2 * gamma + 1) * p.cpr;
   p.stage_bytes = static_cast<uint32_t>(CE * esize);
+  // a multiple of the consumer-warp count: stage s is always consumed by warp
+  // s % kRowWarps, so its mbarrier phases cannot alias
   p.nstages = static_cast<int>(kRingBytes / p.stage_bytes);
   if (p.nstages > kMaxStages) p.nstages = kMaxStages;
+  p.nstages -= p.nstages % kRowWarps;
   const int live_items = rows * p.cpr;
   p.grid = live_items < sms ? live_items : sms;
   if (p.grid < 1) p.grid = 1;
@@ -183,7 +186,7 @@ int run_chain(const Common& a, bool sampling) {
   ap.partials = rp.partials;
   ap.rowstat = reinterpret_cast<RowStat*>(ws + L.rowstat);
   ap.seq = reinterpret_cast<SeqState*>(ws + L.seq);
-  ap.mass = reinterpret_cast<double*>(ws + L.mass);
+  ap.mass = reinterpret_cast<float*>(ws + L.mass);
   ap.out_tokens = a.out_tokens;
   ap.out_num = a.out_num;
   ap.out_debug = sampling ? a.out_debug : nullptr;
@@ -211,10 +214,10 @@ int run_chain(const Common& a, bool sampling) {
   sp.V = a.V;
   sp.CE = pl.CE;
   sp.cpr = pl.cpr;
-  if (launch_pdl(residual_mass_kernel<T>, dim3(pl.cpr, a.B), dim3(kSampleThreads), 0, a.stream, sp) !=
+  if (launch_pdl(residual_mass_kernel<T>, dim3(pl.cpr, a.B), dim3(kMassThreads), 0, a.stream, sp) !=
       cudaSuccess)
     return SPEC_ERR_CUDA;
-  if (launch_pdl(sample_kernel<T>, dim3(a.B), dim3(kSampleThreads), 0, a.stream, sp) != cudaSuccess)
+  if (launch_pdl(sample_kernel<T>, dim3(a.B), dim3(32), 0, a.stream, sp) != cudaSuccess)
     return SPEC_ERR_CUDA;
   return SPEC_OK;
 }
