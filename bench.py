@@ -282,7 +282,8 @@ def run_ours(args):
                    "l2": f"inputs larger than L2: pool of {POOL} rounds x {bytes_mean / 1e6:.1f} MB cycled"},
         "logit_gbs": round(gbs, 1), "frac_of_8tbs": round(gbs / ws_n / NOMINAL_HBM_GBS, 4),
         "frac_of_measured_hbm": round(gbs / ws_n / peak, 4),
-        "roofline": {"bound": "hbm", "kernel": "rowstats_kernel<bf16>", "achieved": round(achieved, 1),
+        "roofline": {"bound": "hbm",
+                     "kernel": "rowstats_kernel<bf16, %s loads>" % os.environ.get("SPECV_ROW_LOADS", "ldg"), "achieved": round(achieved, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback 6.8 TB/s",
                      "traffic": traffic, "bytes_per_launch": bytes_mean,
@@ -473,12 +474,16 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end host-buffer leg")
+    ap.add_argument("--row-loads", choices=("ldg", "tma"), default=None,
+                    help="row-reducer load path (default: the library's default, direct loads)")
     args = ap.parse_args()
     if args.impl == "reference":
         args.steps = 100 if args.steps is None else args.steps
         args.warmup = 3 if args.warmup is None else args.warmup
         run_reference(args)
     else:
+        if args.row_loads:
+            os.environ["SPECV_ROW_LOADS"] = args.row_loads
         args.steps = 20000 if args.steps is None else args.steps
         args.warmup = 20 if args.warmup is None else max(3, args.warmup)
         run_ours(args)

@@ -9,6 +9,7 @@
 // launch latency overlaps the tail of the previous kernel; each one waits for
 // its predecessor's results with griddepcontrol.wait before reading them.
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -27,6 +28,7 @@ constexpr int kMaxDevices = 64;
 
 struct DeviceInfo {
   int sms = 0;
+  int path = kLdg;  // row-reducer load path (SPECV_ROW_LOADS=tma selects kTma)
   bool ready = false;
 };
 DeviceInfo g_dev[kMaxDevices];
@@ -40,12 +42,14 @@ int device_info(DeviceInfo* out) {
   if (!d.ready) {
     if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return SPEC_ERR_CUDA;
-    const int smem = static_cast<int>(kRingBytes);
-    if (cudaFuncSetAttribute(rowstats_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-            cudaSuccess ||
-        cudaFuncSetAttribute(rowstats_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem) != cudaSuccess)
+    const int smem = static_cast<int>(kTmaRingBytes);
+    if (cudaFuncSetAttribute(rowstats_kernel<float, kTma>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem) != cudaSuccess ||
+        cudaFuncSetAttribute(rowstats_kernel<__nv_bfloat16, kTma>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
       return SPEC_ERR_CUDA;
+    const char* env = std::getenv("SPECV_ROW_LOADS");
+    d.path = (env != nullptr && std::strcmp(env, "tma") == 0) ? kTma : kLdg;
     d.ready = true;
   }
   *out = d;
@@ -86,31 +90,27 @@ int check_shape(int B, int gamma, int V) {
   return SPEC_OK;
 }
 
-// Chunk size: 4 KB of logits per chunk (one ring stage), halved while the grid would have
-// fewer than ~8 chunks per SM (small batches), never below kMinChunk elements.
+// Chunk size: 4 KB of logits per chunk (one warp's work item), halved while
+// the grid would have fewer than ~8 chunks per SM (small batches), never below
+// kMinChunk elements.
 struct Plan {
-  int CE, cpr, n_items, nstages;
-  uint32_t stage_bytes;
-  int grid;
+  int CE, cpr, grid;
+  size_t smem;
 };
 
-Plan make_plan(int B, int gamma, int V, size_t esize, int sms, bool sampling) {
+Plan make_plan(int B, int gamma, int V, size_t esize, int sms, bool sampling, int path) {
   Plan p;
   const int rows = B * (sampling ? (2 * gamma + 1) : (gamma + 1));
-  int CE = static_cast<int>(kStageBytesMax / esize);
+  int CE = static_cast<int>(kChunkBytes / esize);
   while (CE > kMinChunk && static_cast<long long>(rows) * ((V + CE - 1) / CE) < 8LL * sms) CE >>= 1;
   p.CE = CE;
   p.cpr = (V + CE - 1) / CE;
-  p.n_items = B * (2 * gamma + 1) * p.cpr;
-  p.stage_bytes = static_cast<uint32_t>(CE * esize);
-  // a multiple of the consumer-warp count: stage s is always consumed by warp
-  // s % kRowWarps, so its mbarrier phases cannot alias
-  p.nstages = static_cast<int>(kRingBytes / p.stage_bytes);
-  if (p.nstages > kMaxStages) p.nstages = kMaxStages;
-  p.nstages -= p.nstages % kRowWarps;
-  const int live_items = rows * p.cpr;
-  p.grid = live_items < sms ? live_items : sms;
+  const long long live_items = static_cast<long long>(rows) * p.cpr;
+  const int per_sm = (path == kLdg) ? 2 : 1;  // CTAs resident per SM
+  const long long want = (live_items + kRowWarps - 1) / kRowWarps;
+  p.grid = static_cast<int>(want < static_cast<long long>(per_sm) * sms ? want : per_sm * sms);
   if (p.grid < 1) p.grid = 1;
+  p.smem = (path == kTma) ? kTmaRingBytes : 0;
   return p;
 }
 
@@ -156,7 +156,7 @@ int run_chain(const Common& a, bool sampling) {
   if (device_info(&dev) != SPEC_OK) return SPEC_ERR_CUDA;
   uint8_t* ws = static_cast<uint8_t*>(a.ws);
   int* status = reinterpret_cast<int*>(ws + L.header);
-  const Plan pl = make_plan(a.B, a.gamma, a.V, sizeof(T), dev.sms, sampling);
+  const Plan pl = make_plan(a.B, a.gamma, a.V, sizeof(T), dev.sms, sampling, dev.path);
 
   RowStatsParams rp;
   rp.target = a.target;
@@ -169,11 +169,11 @@ int run_chain(const Common& a, bool sampling) {
   rp.V = a.V;
   rp.CE = pl.CE;
   rp.cpr = pl.cpr;
-  rp.n_items = pl.n_items;
-  rp.nstages = pl.nstages;
-  rp.stage_bytes = pl.stage_bytes;
   rp.debug = a.debug;
-  rowstats_kernel<T><<<pl.grid, kRowThreads, kRingBytes, a.stream>>>(rp);
+  if (dev.path == kTma)
+    rowstats_kernel<T, kTma><<<pl.grid, kRowThreads, pl.smem, a.stream>>>(rp);
+  else
+    rowstats_kernel<T, kLdg><<<pl.grid, kRowThreads, 0, a.stream>>>(rp);
   if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
   if (a.debug || a.reduce_only) return SPEC_OK;
 

@@ -236,3 +236,45 @@ def test_repeat_calls_are_bitwise_deterministic(sv, dev):
     b = run_sample(sv, d, ws)
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
     assert np.array_equal(a[2], b[2], equal_nan=True)
+
+
+_TMA_CHILD = r"""
+import sys, numpy as np, torch
+sys.path.insert(0, sys.argv[1])
+import speculative_decoding_verification_54_gb300 as sv
+import workloads as wl
+from tests.gpu_util import to_device, run_sample, run_greedy
+torch.cuda.set_device(0)
+out = {}
+for name, kw in (("bf16", dict(B=6, gamma=4, V=3 * 2048 + 24, dtype="bf16", profile="zipf",
+                              temperature=("alternate", 0.0, 0.9))),
+                 ("f32", dict(B=40, gamma=3, V=8192, dtype="f32", temperature=1.1))):
+    inp = wl.make_custom(seed=21, **kw)
+    ws = sv.make_workspace(inp.B, inp.gamma, inp.V)
+    d = to_device(inp, torch.device("cuda:0"))
+    tok, num, dbg, st = run_sample(sv, d, ws)
+    gt, gn, st2 = run_greedy(sv, d, ws)
+    assert st == 0 and st2 == 0
+    out[name + "_tok"], out[name + "_num"], out[name + "_dbg"] = tok, num, dbg
+    out[name + "_gtok"], out[name + "_gnum"] = gt, gn
+np.savez(sys.argv[2], **out)
+"""
+
+
+def test_bulk_copy_load_path_matches_direct_loads(sv, tmp_path):
+    """The TMA bulk-copy staging of the row reducer gives bit-identical results
+    to the default direct-load path (same arithmetic, different loads)."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    res = {}
+    for path in ("ldg", "tma"):
+        f = tmp_path / f"{path}.npz"
+        env = dict(os.environ, SPECV_ROW_LOADS=path)
+        r = subprocess.run([sys.executable, "-c", _TMA_CHILD, root, str(f)], env=env, cwd=root,
+                           capture_output=True, text=True, timeout=600)
+        assert r.returncode == 0, r.stderr[-2000:]
+        res[path] = dict(np.load(f))
+    for k in res["ldg"]:
+        assert np.array_equal(res["ldg"][k], res["tma"][k], equal_nan=True), k
