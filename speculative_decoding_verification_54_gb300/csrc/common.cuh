@@ -24,7 +24,11 @@ constexpr long long kWaitLimitCyclesShort = 2000000LL;  // forced-timeout self-t
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kNegHuge = -3.0e38f;  // stands for -inf in scaled maxima
 
-// sequence modes written by the accept kernel
+// completion counters each sit on their own 128-byte line (no atomic
+// contention between sequences)
+constexpr int kCounterStride = 32;
+
+// sequence modes written by the deciding warp
 constexpr int kModeGreedy = 0;    // fully decided (greedy or greedy row)
 constexpr int kModeResidual = 1;  // sample position n from max(0, p_n - q_n)
 constexpr int kModeBonus = 2;     // all accepted: sample the bonus from p_gamma

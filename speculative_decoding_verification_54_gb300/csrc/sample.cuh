@@ -1,43 +1,50 @@
-// sample.cuh — residual normaliser and inverse-CDF sampler.
+// sample.cuh — the tail kernel: decide, residual normaliser, inverse-CDF draw.
 //
-// After a rejection at position n the token is drawn from
-// w(x) = max(0, p_n(x) - q_n(x)) / Z ("Gemma 4 Multi-Token Prediction (MTP)
-// 深度解析" §2.2; "自投机解码：层跳过与拒绝采样实现大模型推理加速" §3.2), and after a
-// fully accepted draft from p_gamma (the bonus).  The draw is an inverse CDF
-// in ascending vocabulary order: the smallest k with sum_{x<=k} w(x) > u*Z.
-//
-// Two levels keep it parallel:
-//   residual_mass_kernel  one CTA per (sequence, chunk): the mass of w over the
-//                         chunk (bonus masses come from the row partials);
-//   sample_kernel         one warp per sequence: a scan over the chunk masses
-//                         picks the chunk, a scan over that chunk's elements
-//                         picks the token.
-// Element weights are fp32; running sums across lanes and chunks are fp64,
-// which on GB300 is kept to a few dozen operations per lane.
+// tail_kernel, grid (parts, B), one sequence per blockIdx.y.  Every CTA of a
+// sequence folds the sequence's row partials (a few KB from L2) and takes the
+// acceptance decision (decide.cuh) — identical in every CTA, so no CTA waits
+// on another; part 0 writes the outputs.  Then, when the sequence samples:
+//   * after a rejection at position n the token is drawn from
+//     w(x) = max(0, p_n(x) - q_n(x)) / Z ("Gemma 4 Multi-Token Prediction
+//     (MTP) 深度解析" §2.2; "自投机解码：层跳过与拒绝采样实现大模型推理加速" §3.2):
+//     each CTA computes the masses of w over its share of the chunks, one warp
+//     per chunk over the row pair;
+//   * after a fully accepted draft the bonus is drawn from p_gamma ("第 8 章
+//     投机解码：一次前向，验证好几个字", 多出来的那一个 token 从哪来): the chunk masses
+//     come straight from the row partials.
+// The last CTA of the sequence to finish (a per-sequence counter, reset by
+// that CTA) draws the token by inverse CDF in ascending vocabulary order, the
+// smallest k with sum_{x<=k} w(x) > u*Z: one warp scans the chunk masses to
+// pick the chunk, then scans that chunk's entries.  Element weights are fp32;
+// running sums across lanes and chunks are fp64, a few dozen operations per
+// lane since FP64 is slow on GB300.
 #pragma once
 
 #include <cfloat>
 
 #include "common.cuh"
+#include "decide.cuh"
+#include "rowstats.cuh"
 
 namespace specv {
 
-constexpr int kMassThreads = 256;
+constexpr int kTailThreads = 512;
+constexpr int kTailWarps = kTailThreads / 32;
 
 struct SampleParams {
   const void* target;
   const void* draft;
   const float* u_resample;
-  const float4* partials;
-  const RowStat* rowstat;
-  const SeqState* seq;
-  float* mass;
-  int32_t* out_tokens;
+  const float4* partials;  // [B*(2*gamma+1)*cpr] from the row reducer
+  float* mass;             // [B*cpr] chunk masses of the selected row (pair)
+  int* tail_done;          // [B*kCounterStride] CTAs finished per sequence
+  DecideParams dp;
   int B, gamma, V, CE, cpr;
 };
 
 // Weight of one vocabulary entry of the selected row (pair), in the units of
-// the chunk masses: residual -> max(0, p - q); bonus -> p * S (units of 2^mk).
+// the chunk masses: residual -> max(0, p - q); plain row -> p * S (units of
+// 2^mk).
 struct WeightFn {
   float ks, mkp, mkq, invSp, invSq;
   bool residual;
@@ -51,23 +58,15 @@ struct WeightFn {
   }
 };
 
-__device__ __forceinline__ WeightFn make_weight(const SampleParams& p, int b, int n, int rowp,
-                                                bool residual, float ks) {
-  const int slots = 2 * p.gamma + 1;
+__device__ __forceinline__ WeightFn make_weight(const RowStat& rp, const RowStat& rq, bool residual,
+                                                float ks) {
   WeightFn f;
   f.ks = ks;
   f.residual = residual;
-  const RowStat rp = p.rowstat[b * slots + rowp];
   f.mkp = rp.mk;
   f.invSp = ex2(-rp.lse2);
-  if (residual) {
-    const RowStat rq = p.rowstat[b * slots + p.gamma + 1 + n];
-    f.mkq = rq.mk;
-    f.invSq = ex2(-rq.lse2);
-  } else {
-    f.mkq = 0.f;
-    f.invSq = 0.f;
-  }
+  f.mkq = residual ? rq.mk : 0.f;
+  f.invSq = residual ? ex2(-rq.lse2) : 0.f;
   return f;
 }
 
@@ -77,190 +76,274 @@ __device__ __forceinline__ const uint4* chunk_vec(const void* base, size_t row, 
                                         (row * V + static_cast<size_t>(c) * CE) * sizeof(T));
 }
 
-// Warp-inclusive scan of one double per lane.
-__device__ __forceinline__ double warp_scan_incl(double v) {
+// Two-float numbers (hi + lo, |lo| <= ulp(hi)/2): sums to about 2^-44
+// relative in fp32 arithmetic, since FP64 is slow on GB300.
+struct F2 {
+  float hi, lo;
+};
+__device__ __forceinline__ F2 f2_add(F2 a, F2 b) {
+  const float s = a.hi + b.hi;
+  const float bb = s - a.hi;
+  const float e = (a.hi - (s - bb)) + (b.hi - bb);  // exact error of s
+  const float t = e + a.lo + b.lo;
+  const float h = s + t;
+  return F2{h, t - (h - s)};
+}
+__device__ __forceinline__ F2 f2_from(float x) { return F2{x, 0.f}; }
+__device__ __forceinline__ F2 f2_mul_f(F2 a, float u) {  // a * u
+  const float h = a.hi * u;
+  const float l = fmaf(a.hi, u, -h) + a.lo * u;
+  const float r = h + l;
+  return F2{r, l - (r - h)};
+}
+__device__ __forceinline__ F2 f2_sub(F2 a, F2 b) { return f2_add(a, F2{-b.hi, -b.lo}); }
+__device__ __forceinline__ bool f2_gt(F2 a, F2 b) { return (a.hi - b.hi) + (a.lo - b.lo) > 0.f; }
+__device__ __forceinline__ F2 f2_shfl_up(F2 v, int off) {
+  return F2{__shfl_up_sync(0xffffffffu, v.hi, off), __shfl_up_sync(0xffffffffu, v.lo, off)};
+}
+__device__ __forceinline__ F2 f2_shfl(F2 v, int src) {
+  return F2{__shfl_sync(0xffffffffu, v.hi, src), __shfl_sync(0xffffffffu, v.lo, src)};
+}
+// Warp-inclusive scan of one two-float per lane.
+__device__ __forceinline__ F2 warp_scan_incl(F2 v) {
   const int lane = threadIdx.x & 31;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
-    const double o = __shfl_up_sync(0xffffffffu, v, off);
-    if (lane >= off) v += o;
+    const F2 o = f2_shfl_up(v, off);
+    if (lane >= off) v = f2_add(v, o);
   }
   return v;
 }
 
-// ---------------------------------------------------------------------------
-// K3: residual chunk masses
-// ---------------------------------------------------------------------------
+// Mass of w over one chunk (warp-wide; lanes hold vectors lane, lane+32, ...).
 template <typename T>
-__global__ void __launch_bounds__(kMassThreads) residual_mass_kernel(const SampleParams p) {
-  __shared__ float warp_part[kMassThreads / 32];
-  grid_dep_wait();
-  const int b = blockIdx.y, c = blockIdx.x;
-  const SeqState s = p.seq[b];
-  if (s.mode != kModeResidual) return;
+__device__ __forceinline__ float chunk_mass(const SampleParams& p, const WeightFn& f, int b, int n,
+                                            int c) {
   constexpr int P = Elt<T>::kPerVec;
-  const WeightFn f = make_weight(p, b, s.n, s.n, true, s.ks);
-  const int g = p.gamma;
-  const uint4* vp = chunk_vec<T>(p.target, static_cast<size_t>(b) * (g + 1) + s.n, p.V, c, p.CE);
-  const uint4* vq = chunk_vec<T>(p.draft, static_cast<size_t>(b) * g + s.n, p.V, c, p.CE);
-  const int len = min(p.CE, p.V - c * p.CE);
-  const int nvec = len / P;
-  float a0 = 0.f, a1 = 0.f;
-  for (int i = threadIdx.x; i < nvec; i += kMassThreads) {
-    float xp[P], xq[P], w[P];
-    Elt<T>::unpack(vp[i], xp);
-    Elt<T>::unpack(vq[i], xq);
+  const int lane = threadIdx.x & 31, g = p.gamma;
+  const uint4* vp = chunk_vec<T>(p.target, static_cast<size_t>(b) * (g + 1) + n, p.V, c, p.CE);
+  const uint4* vq = chunk_vec<T>(p.draft, static_cast<size_t>(b) * g + n, p.V, c, p.CE);
+  const int nvec = min(p.CE, p.V - c * p.CE) / P;
+  uint4 a[kVecPerLane], q[kVecPerLane];
 #pragma unroll
-    for (int j = 0; j < P; ++j) w[j] = f(xp[j], xq[j]);
-    float t0 = 0.f, t1 = 0.f;
-#pragma unroll
-    for (int j = 0; j < P / 2; ++j) {
-      t0 += w[j];
-      t1 += w[P / 2 + j];
-    }
-    a0 += t0;
-    a1 += t1;
+  for (int j = 0; j < kVecPerLane; ++j) {
+    const int k = lane + 32 * j;
+    a[j] = (k < nvec) ? __ldg(vp + k) : neg_inf_vec<T>();
+    q[j] = (k < nvec) ? __ldg(vq + k) : neg_inf_vec<T>();
   }
-  float v = a0 + a1;
+  float acc = 0.f;
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-  if ((threadIdx.x & 31) == 0) warp_part[threadIdx.x >> 5] = v;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float sum = 0.f, cmp = 0.f;
-    for (int w = 0; w < kMassThreads / 32; ++w) neumaier_add(sum, cmp, warp_part[w]);
-    p.mass[static_cast<size_t>(b) * p.cpr + c] = sum + cmp;
+  for (int j = 0; j < kVecPerLane; ++j) {
+    float xp[P], xq[P];
+    Elt<T>::unpack(a[j], xp);
+    Elt<T>::unpack(q[j], xq);
+    float t = 0.f;
+#pragma unroll
+    for (int k = 0; k < P; ++k) t += f(xp[k], xq[k]);
+    acc += t;
   }
+  return warp_sum(acc);
 }
 
-// ---------------------------------------------------------------------------
-// K4: the inverse-CDF draw, one warp per sequence
-// ---------------------------------------------------------------------------
+// The inverse-CDF draw for sequence b (warp-wide, one warp of the last CTA).
+// rs: the sequence's combined rows; s: its decision.
 template <typename T>
-__global__ void __launch_bounds__(32) sample_kernel(const SampleParams p) {
-  grid_dep_wait();
-  const int b = blockIdx.x, lane = threadIdx.x;
-  const SeqState s = p.seq[b];
-  if (s.mode != kModeResidual && s.mode != kModeBonus) return;
+__device__ __noinline__ void draw_token(const SampleParams& p, int b, const SeqState s,
+                                        const RowStat* rs) {
+  constexpr int P = Elt<T>::kPerVec;
+  const int lane = threadIdx.x & 31;
   const int g = p.gamma, slots = 2 * g + 1;
   float* mass = p.mass + static_cast<size_t>(b) * p.cpr;
   const int per = (p.cpr + 31) / 32;
   const int c0 = min(p.cpr, lane * per), c1 = min(p.cpr, c0 + per);
-
   bool residual = (s.mode == kModeResidual);
   const int rowp = residual ? s.n : g;
 
   // ---- level 1: which chunk (lane-contiguous chunk ranges) ----
-  double lsum = 0.0;
-  for (int c = c0; c < c1; ++c) lsum += static_cast<double>(mass[c]);
-  double incl = warp_scan_incl(lsum);
-  double Z = __shfl_sync(0xffffffffu, incl, 31);
-  if (residual && !(Z > 0.0)) {
+  F2 lsum = f2_from(0.f);
+#pragma unroll 4
+  for (int c = c0; c < c1; ++c) lsum = f2_add(lsum, f2_from(__ldcg(mass + c)));
+  F2 incl = warp_scan_incl(lsum);
+  F2 Z = f2_shfl(incl, 31);
+  if (residual && !(Z.hi > 0.f)) {
     // Z == 0 cannot happen in exact arithmetic; if rounding produces it, draw
     // from p_n itself (chunk masses from the row partials)
-    const float4* P = p.partials + static_cast<size_t>(b * slots + s.n) * p.cpr;
-    const float mk = p.rowstat[b * slots + s.n].mk;
-    lsum = 0.0;
+    const float4* P4 = p.partials + static_cast<size_t>(b * slots + s.n) * p.cpr;
+    const float mk = rs[s.n].mk;
+    lsum = f2_from(0.f);
     for (int c = c0; c < c1; ++c) {
-      const float4 q = P[c];
+      const float4 q = __ldcg(P4 + c);
       mass[c] = q.y * ex2(q.w - mk);
-      lsum += static_cast<double>(mass[c]);
+      lsum = f2_add(lsum, f2_from(mass[c]));
     }
     incl = warp_scan_incl(lsum);
-    Z = __shfl_sync(0xffffffffu, incl, 31);
+    Z = f2_shfl(incl, 31);
     residual = false;  // weights of target row n as a plain row
   }
-  const double target = static_cast<double>(p.u_resample[b]) * Z;
-  const unsigned over = __ballot_sync(0xffffffffu, incl > target);
+  const F2 target = f2_mul_f(Z, p.u_resample[b]);
+  const unsigned over = __ballot_sync(0xffffffffu, f2_gt(incl, target));
   int chunk = -1;
-  double local = DBL_MAX;
+  F2 local = F2{FLT_MAX, 0.f};
   if (over) {
     const int L = __ffs(over) - 1;
     if (lane == L) {
-      double run = incl - lsum;
+      F2 run = f2_sub(incl, lsum);
       for (int c = c0; c < c1; ++c) {
-        const double mc = static_cast<double>(mass[c]);
-        if (run + mc > target) {
+        const F2 nxt = f2_add(run, f2_from(__ldcg(mass + c)));
+        if (f2_gt(nxt, target)) {
           chunk = c;
-          local = target - run;
+          local = f2_sub(target, run);
           break;
         }
-        run += mc;
+        run = nxt;
       }
       if (chunk < 0) {  // rounding inside the lane: its last nonzero chunk
         for (int c = c1 - 1; c >= c0; --c)
-          if (mass[c] > 0.f) {
+          if (__ldcg(mass + c) > 0.f) {
             chunk = c;
             break;
           }
       }
     }
     chunk = __shfl_sync(0xffffffffu, chunk, L);
-    local = __shfl_sync(0xffffffffu, local, L);
+    local = f2_shfl(local, L);
   }
   if (chunk < 0) {  // u*Z at or beyond the total: the last nonzero chunk
     int last = -1;
     for (int c = c0; c < c1; ++c)
-      if (mass[c] > 0.f) last = c;
+      if (__ldcg(mass + c) > 0.f) last = c;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, off));
     chunk = last < 0 ? 0 : last;
-    local = DBL_MAX;
+    local = F2{FLT_MAX, 0.f};
   }
 
-  // ---- level 2: which token inside the chunk (lane-contiguous vectors) ----
-  const WeightFn f = make_weight(p, b, s.n, rowp, residual, s.ks);
-  constexpr int P = Elt<T>::kPerVec;
+  // ---- level 2: which entry inside the chunk.  The chunk's 256 vectors are
+  // taken in two halves; in each, lane l holds the contiguous vectors
+  // [h*128 + 4l, h*128 + 4l + 4) in registers, so the running sum follows
+  // vocabulary order across lanes. ----
+  constexpr int kHalfVec = 4;
+  const WeightFn f = make_weight(rs[rowp], rs[g + 1 + (residual ? s.n : 0)], residual, s.ks);
   const uint4* vp = chunk_vec<T>(p.target, static_cast<size_t>(b) * (g + 1) + rowp, p.V, chunk, p.CE);
-  const uint4* vq = residual ? chunk_vec<T>(p.draft, static_cast<size_t>(b) * g + s.n, p.V, chunk, p.CE)
-                             : nullptr;
-  const int len = min(p.CE, p.V - chunk * p.CE);
-  const int nvec = len / P;
-  const int vper = (nvec + 31) / 32;
-  const int v0 = min(nvec, lane * vper), v1 = min(nvec, v0 + vper);
-  float my = 0.f;
-  int last_nz = -1;
-  for (int i = v0; i < v1; ++i) {
-    float xp[P], xq[P];
-    Elt<T>::unpack(vp[i], xp);
-    if (residual) Elt<T>::unpack(vq[i], xq);
-    float t = 0.f;
+  const uint4* vq = chunk_vec<T>(residual ? p.draft : p.target,
+                                 static_cast<size_t>(b) * (residual ? g : g + 1) + (residual ? s.n : rowp),
+                                 p.V, chunk, p.CE);
+  const int nvec = min(p.CE, p.V - chunk * p.CE) / P;
+  F2 base = f2_from(0.f);
+  int tok = -1, last_all = -1;
+#pragma unroll 1
+  for (int h = 0; h < 2 && tok < 0; ++h) {
+    const int v0 = h * (32 * kHalfVec) + lane * kHalfVec;
+    uint4 a[kHalfVec], q[kHalfVec];
 #pragma unroll
-    for (int j = 0; j < P; ++j) {
-      const float w = f(xp[j], residual ? xq[j] : 0.f);
-      t += w;
-      if (w > 0.f) last_nz = i * P + j;
+    for (int j = 0; j < kHalfVec; ++j) {
+      const int i = v0 + j;
+      a[j] = (i < nvec) ? __ldg(vp + i) : neg_inf_vec<T>();
+      q[j] = (i < nvec && residual) ? __ldg(vq + i) : neg_inf_vec<T>();
     }
-    my += t;
-  }
-  const double cincl = warp_scan_incl(static_cast<double>(my));
-  const unsigned cover = __ballot_sync(0xffffffffu, cincl > local);
-  int tok = -1;
-  if (cover) {
-    const int L = __ffs(cover) - 1;
-    if (lane == L) {
-      double run = cincl - static_cast<double>(my);
-      for (int i = v0; i < v1 && tok < 0; ++i) {
-        float xp[P], xq[P];
-        Elt<T>::unpack(vp[i], xp);
-        if (residual) Elt<T>::unpack(vq[i], xq);
+    F2 my = f2_from(0.f);
+    int last_nz = -1;
 #pragma unroll
-        for (int j = 0; j < P; ++j) {
-          const float w = f(xp[j], residual ? xq[j] : 0.f);
-          run += static_cast<double>(w);
-          if (tok < 0 && run > local) tok = i * P + j;
-        }
+    for (int j = 0; j < kHalfVec; ++j) {
+      float xp[P], xq[P];
+      Elt<T>::unpack(a[j], xp);
+      Elt<T>::unpack(q[j], xq);
+      float t = 0.f;
+#pragma unroll
+      for (int k = 0; k < P; ++k) {
+        const float w = f(xp[k], xq[k]);
+        t += w;
+        if (w > 0.f) last_nz = (v0 + j) * P + k;
       }
-      if (tok < 0) tok = last_nz;  // rounding inside the lane
+      my = f2_add(my, f2_from(t));
     }
-    tok = __shfl_sync(0xffffffffu, tok, L);
+    const F2 cincl = f2_add(warp_scan_incl(my), base);
+    const unsigned cover = __ballot_sync(0xffffffffu, f2_gt(cincl, local));
+    if (cover) {
+      const int L = __ffs(cover) - 1;
+      if (lane == L) {
+        F2 run = f2_sub(cincl, my);
+#pragma unroll
+        for (int j = 0; j < kHalfVec; ++j) {
+          float xp[P], xq[P];
+          Elt<T>::unpack(a[j], xp);
+          Elt<T>::unpack(q[j], xq);
+#pragma unroll
+          for (int k = 0; k < P; ++k) {
+            run = f2_add(run, f2_from(f(xp[k], xq[k])));
+            if (tok < 0 && f2_gt(run, local)) tok = (v0 + j) * P + k;
+          }
+        }
+        if (tok < 0) tok = last_nz;  // rounding inside the lane
+      }
+      tok = __shfl_sync(0xffffffffu, tok, L);
+    }
+    base = f2_shfl(cincl, 31);
+    last_all = max(last_all, last_nz);
   }
   if (tok < 0) {  // beyond the chunk total: its last nonzero entry
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) last_nz = max(last_nz, __shfl_xor_sync(0xffffffffu, last_nz, off));
-    tok = last_nz < 0 ? 0 : last_nz;
+    for (int off = 16; off > 0; off >>= 1) last_all = max(last_all, __shfl_xor_sync(0xffffffffu, last_all, off));
+    tok = last_all < 0 ? 0 : last_all;
   }
-  if (lane == 0) p.out_tokens[b * (g + 1) + s.n] = chunk * p.CE + tok;
+  if (lane == 0) p.dp.out_tokens[b * (g + 1) + s.n] = chunk * p.CE + tok;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kTailThreads, 1) tail_kernel(const __grid_constant__ SampleParams p) {
+  __shared__ RowStat rs[2 * 31 + 1];  // gamma <= 31
+  __shared__ SeqState s_seq;
+  __shared__ int s_last;
+  const int b = blockIdx.y, part = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = p.gamma, slots = 2 * g + 1;
+  const bool greedy = (p.dp.temperature == nullptr) || seq_is_greedy(p.dp.temperature, b);
+  const int nrows = greedy ? g + 1 : slots;
+  // inputs of the decision do not depend on the row reducer: load them first
+  DecideIn din;
+  if (warp == 0) din = prefetch_decide<T>(p.dp, b, greedy);
+  grid_dep_wait();
+
+  // ---- combine the sequence's rows, one warp per row ----
+  for (int r = warp; r < nrows; r += kTailWarps) {
+    const RowStat st = combine_row(p.partials + static_cast<size_t>(b * slots + r) * p.cpr, p.cpr, !greedy);
+    if (lane == 0) rs[r] = st;
+  }
+  __syncthreads();
+  if (warp == 0) decide_sequence<T>(p.dp, b, rs, din, part == 0, &s_seq);
+  __syncthreads();
+  const SeqState s = s_seq;
+  if (s.mode != kModeResidual && s.mode != kModeBonus) return;
+
+  // ---- chunk masses of the row (pair) to draw from, this CTA's share ----
+  const int per = (p.cpr + gridDim.x - 1) / gridDim.x;
+  const int c0 = min(p.cpr, part * per), c1 = min(p.cpr, c0 + per);
+  float* mass = p.mass + static_cast<size_t>(b) * p.cpr;
+  if (s.mode == kModeResidual) {
+    const WeightFn f = make_weight(rs[s.n], rs[g + 1 + s.n], true, s.ks);
+    for (int c = c0 + warp; c < c1; c += kTailWarps) {
+      const float m = chunk_mass<T>(p, f, b, s.n, c);
+      if (lane == 0) mass[c] = m;
+    }
+  } else {  // bonus: masses of p_gamma from the row partials
+    const float4* P = p.partials + static_cast<size_t>(b * slots + g) * p.cpr;
+    const float mk = rs[g].mk;
+    for (int c = c0 + threadIdx.x; c < c1; c += kTailThreads) {
+      const float4 q = __ldcg(P + c);
+      mass[c] = q.y * ex2(q.w - mk);
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const int old = atomicAdd(&p.tail_done[b * kCounterStride], 1);
+    s_last = (old == static_cast<int>(gridDim.x) - 1);
+    if (s_last) p.tail_done[b * kCounterStride] = 0;  // ready for the next call
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  if (warp == 0) draw_token<T>(p, b, s, rs);
 }
 
 }  // namespace specv

@@ -2,18 +2,19 @@
 // layout and kernel launches behind the C ABI declared in spec_verify.h.
 //
 // Launch chain of one call (all on the caller's stream):
-//   greedy:  rowstats (argmax of target rows)  -> accept
-//   sample:  rowstats (softmax stats of target + draft rows) -> accept
-//            -> residual_mass -> sample
-// Later kernels are launched with programmatic stream serialization so their
-// launch latency overlaps the tail of the previous kernel; each one waits for
-// its predecessor's results with griddepcontrol.wait before reading them.
+//   rowstats  chunk partials of every row the call needs (argmax for greedy
+//             target rows, softmax statistics for sampled rows)
+//   tail      per sequence: row combine, acceptance decision, and for sampled
+//             sequences the residual / bonus chunk masses and the draw
+// The tail kernel is launched with programmatic stream serialization so its
+// launch latency overlaps the row reducer; it waits for the reducer's results
+// with griddepcontrol.wait before reading them.
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
 
-#include "accept.cuh"
+#include "decide.cuh"
 #include "common.cuh"
 #include "rowstats.cuh"
 #include "sample.cuh"
@@ -57,7 +58,7 @@ int device_info(DeviceInfo* out) {
 }
 
 struct Layout {
-  size_t header, partials, rowstat, seq, mass, total;
+  size_t header, partials, mass, tail_done, total;
 };
 
 // Offsets of the workspace regions for a call with (B, gamma, V); sized for
@@ -71,12 +72,10 @@ Layout layout(int B, int gamma, int V) {
   off += align_up(sizeof(WsHeader), 256);
   L.partials = off;
   off += align_up(slots * cpr * sizeof(float4), 256);
-  L.rowstat = off;
-  off += align_up(slots * sizeof(RowStat), 256);
-  L.seq = off;
-  off += align_up(static_cast<size_t>(B) * sizeof(SeqState), 256);
   L.mass = off;
   off += align_up(static_cast<size_t>(B) * cpr * sizeof(float), 256);
+  L.tail_done = off;  // per-sequence counters: zero when no call is running
+  off += align_up(static_cast<size_t>(B) * kCounterStride * sizeof(int), 256);
   L.total = off;
   return L;
 }
@@ -177,47 +176,37 @@ int run_chain(const Common& a, bool sampling) {
   if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
   if (a.debug || a.reduce_only) return SPEC_OK;
 
-  AcceptParams ap;
-  ap.target = a.target;
-  ap.draft = a.draft;
-  ap.draft_tokens = a.draft_tokens;
-  ap.temperature = sampling ? a.temperature : nullptr;
-  ap.u_accept = a.u_accept;
-  ap.partials = rp.partials;
-  ap.rowstat = reinterpret_cast<RowStat*>(ws + L.rowstat);
-  ap.seq = reinterpret_cast<SeqState*>(ws + L.seq);
-  ap.mass = reinterpret_cast<float*>(ws + L.mass);
-  ap.out_tokens = a.out_tokens;
-  ap.out_num = a.out_num;
-  ap.out_debug = sampling ? a.out_debug : nullptr;
-  ap.status = status;
-  ap.B = a.B;
-  ap.gamma = a.gamma;
-  ap.V = a.V;
-  ap.CE = pl.CE;
-  ap.cpr = pl.cpr;
-  if (launch_pdl(accept_kernel<T>, dim3(a.B), dim3(kAcceptThreads), 0, a.stream, ap) != cudaSuccess)
-    return SPEC_ERR_CUDA;
-  if (!sampling) return SPEC_OK;
-
   SampleParams sp;
   sp.target = a.target;
-  sp.draft = a.draft;
+  sp.draft = rp.draft;
   sp.u_resample = a.u_resample;
   sp.partials = rp.partials;
-  sp.rowstat = ap.rowstat;
-  sp.seq = ap.seq;
-  sp.mass = ap.mass;
-  sp.out_tokens = a.out_tokens;
+  sp.mass = reinterpret_cast<float*>(ws + L.mass);
+  sp.tail_done = reinterpret_cast<int*>(ws + L.tail_done);
   sp.B = a.B;
   sp.gamma = a.gamma;
   sp.V = a.V;
   sp.CE = pl.CE;
   sp.cpr = pl.cpr;
-  if (launch_pdl(residual_mass_kernel<T>, dim3(pl.cpr, a.B), dim3(kMassThreads), 0, a.stream, sp) !=
-      cudaSuccess)
-    return SPEC_ERR_CUDA;
-  if (launch_pdl(sample_kernel<T>, dim3(a.B), dim3(32), 0, a.stream, sp) != cudaSuccess)
+  DecideParams& dp = sp.dp;
+  dp.target = a.target;
+  dp.draft = rp.draft;
+  dp.draft_tokens = a.draft_tokens;
+  dp.temperature = rp.temperature;
+  dp.u_accept = a.u_accept;
+  dp.out_tokens = a.out_tokens;
+  dp.out_num = a.out_num;
+  dp.out_debug = sampling ? a.out_debug : nullptr;
+  dp.status = status;
+  dp.gamma = a.gamma;
+  dp.V = a.V;
+  // parts per sequence: about two CTAs per SM over the batch (at most 16);
+  // greedy calls need one (no residual pass)
+  int parts = sampling ? (2 * dev.sms + a.B - 1) / a.B : 1;
+  if (parts > 16) parts = 16;
+  if (parts > pl.cpr) parts = pl.cpr;
+  if (parts < 1) parts = 1;
+  if (launch_pdl(tail_kernel<T>, dim3(parts, a.B), dim3(kTailThreads), 0, a.stream, sp) != cudaSuccess)
     return SPEC_ERR_CUDA;
   return SPEC_OK;
 }
