@@ -132,6 +132,35 @@ int spec_verify_sample_reduce_only(const void *target_logits, const void *draft_
                                    size_t workspace_bytes, void *stream);
 
 /*
+ * spec_verify_sample without a workspace, for callers that cannot allocate
+ * device memory (the pages have no counterpart: this is an integration aid).
+ * Such callers include plugins or custom ops inside an inference engine that
+ * owns all device memory through its own pool, and decode loops where a
+ * cudaMalloc could synchronise the device and stall other streams.
+ *
+ * Same arguments and results as spec_verify_sample, minus the workspace.  The
+ * scratch is a fixed 16 MiB array built into the library; every GPU that
+ * loads the library holds it until the process exits.  Problems whose
+ * workspace (spec_verify_workspace_bytes) exceeds 16 MiB are rejected with
+ * SPEC_ERR_WORKSPACE (B=128, gamma=8, V=262144 needs about 9 MB).
+ *
+ * - The first call on a device, with that device current, looks up the
+ *   array's address and zeroes it (a synchronous cudaMemset); make that first
+ *   call before any stream capture.  Nothing is ever allocated or freed.
+ * - All calls share the one array: calls that overlap on the GPU (other
+ *   streams, other host threads) race and give wrong tokens.  Serialise them.
+ * - Device-side errors (a draft token outside [0, V), a wait that ran out)
+ *   are recorded in the built-in scratch but cannot be read back through
+ *   this entry point; host-side checks return codes as usual.
+ */
+int spec_verify_sample_noalloc(const void *target_logits, const void *draft_logits,
+                               spec_dtype dt, const int32_t *draft_tokens,
+                               const float *temperature, const float *u_accept,
+                               const float *u_resample, int B, int gamma, int V,
+                               int32_t *out_tokens, int32_t *out_num_accepted,
+                               float *out_debug, void *stream);
+
+/*
  * Synchronise `stream`, then return the device-side status recorded in
  * `workspace` since the last call (SPEC_OK, SPEC_ERR_TIMEOUT or
  * SPEC_ERR_DEVICE_INPUT) and clear it.  Returns SPEC_ERR_CUDA if the

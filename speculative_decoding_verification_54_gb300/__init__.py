@@ -25,6 +25,7 @@ from .binding import (  # noqa: F401
     make_workspace,
     spec_verify_greedy,
     spec_verify_sample,
+    spec_verify_sample_noalloc,
     spec_verify_sample_reduce_only,
     spec_verify_selftest_timeout,
     spec_verify_status,

@@ -28,6 +28,7 @@ EXPORTED = (
     "spec_verify_workspace_bytes", "spec_verify_workspace_init", "spec_verify_greedy",
     "spec_verify_sample", "spec_verify_status", "spec_verify_error_string",
     "spec_verify_version", "spec_verify_selftest_timeout", "spec_verify_sample_reduce_only",
+    "spec_verify_sample_noalloc",
 )
 
 
@@ -60,6 +61,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.spec_verify_sample.argtypes = [_vp, _vp, _i, _vp, _vp, _vp, _vp, _i, _i, _i,
                                        _vp, _vp, _vp, _vp, _sz, _vp]
     lib.spec_verify_sample_reduce_only.argtypes = list(lib.spec_verify_sample.argtypes)
+    lib.spec_verify_sample_noalloc.argtypes = [_vp, _vp, _i, _vp, _vp, _vp, _vp, _i, _i, _i,
+                                               _vp, _vp, _vp, _vp]
     lib.spec_verify_status.argtypes = [_vp, _vp]
     lib.spec_verify_error_string.argtypes = [_i]
     lib.spec_verify_error_string.restype = ctypes.c_char_p
@@ -180,6 +183,21 @@ def spec_verify_sample_reduce_only(target_logits, draft_logits, draft_tokens, te
         _ptr(temperature), _ptr(u_accept), _ptr(u_resample), B, g1 - 1, V, _ptr(out_tokens),
         _ptr(out_num_accepted), _ptr(out_debug), _ptr(workspace), _nbytes(workspace),
         _stream(stream)), "spec_verify_sample_reduce_only")
+
+
+def spec_verify_sample_noalloc(target_logits, draft_logits, draft_tokens, temperature, u_accept,
+                               u_resample, out_tokens, out_num_accepted, out_debug=None,
+                               stream=None) -> None:
+    """spec_verify_sample for callers that cannot allocate device memory: no
+    workspace, the library's built-in 16 MiB scratch instead.  Calls must not
+    overlap on the GPU (they share that scratch)."""
+    B, g1, V = target_logits.shape
+    if draft_logits.dtype != target_logits.dtype:
+        raise SpecVerifyError(SPEC_ERR_UNSUPPORTED, "target and draft logits differ in dtype")
+    _check(load().spec_verify_sample_noalloc(
+        _ptr(target_logits), _ptr(draft_logits), _dtype_code(target_logits), _ptr(draft_tokens),
+        _ptr(temperature), _ptr(u_accept), _ptr(u_resample), B, g1 - 1, V, _ptr(out_tokens),
+        _ptr(out_num_accepted), _ptr(out_debug), _stream(stream)), "spec_verify_sample_noalloc")
 
 
 def spec_verify_status(workspace, stream=None) -> int:

@@ -364,3 +364,76 @@ int spec_verify_selftest_timeout(void* workspace, size_t workspace_bytes, void* 
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Entry point for callers that cannot allocate device memory.
+//
+// Some callers may not call cudaMalloc at all: a plugin or custom op inside an
+// inference engine that owns every byte of device memory through its own
+// pool, or a latency-critical decode loop where an allocation could
+// synchronise the device and stall the other streams.  For them
+// spec_verify_sample_noalloc keeps its scratch in the array below, a fixed
+// 16 MiB in every GPU that loads this library, held until the process exits.
+// The caller still passes all inputs and outputs.
+// ---------------------------------------------------------------------------
+namespace {
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;
+}  // namespace
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+struct NoAllocDevice {
+  void* ptr = nullptr;  // device address of g_noalloc_scratch on this device
+  bool ready = false;
+};
+NoAllocDevice g_noalloc[kMaxDevices];
+std::mutex g_noalloc_mu;
+
+// Once per device, with that device current: look up the array's device
+// address (its name is only a stand-in in host code) and zero it.
+int noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SPEC_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  NoAllocDevice& d = g_noalloc[dev];
+  if (!d.ready) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return SPEC_ERR_CUDA;
+    if (cudaMemset(p, 0, kNoAllocScratchBytes) != cudaSuccess) return SPEC_ERR_CUDA;
+    d.ptr = p;
+    d.ready = true;
+  }
+  *out = d.ptr;
+  return SPEC_OK;
+}
+}  // namespace
+
+extern "C" int spec_verify_sample_noalloc(const void* target_logits, const void* draft_logits,
+                                          spec_dtype dt, const int32_t* draft_tokens,
+                                          const float* temperature, const float* u_accept,
+                                          const float* u_resample, int B, int gamma, int V,
+                                          int32_t* out_tokens, int32_t* out_num_accepted,
+                                          float* out_debug, void* stream) {
+  // the same checks as spec_verify_sample, before any CUDA call
+  if (target_logits == nullptr || draft_logits == nullptr || draft_tokens == nullptr ||
+      temperature == nullptr || u_accept == nullptr || u_resample == nullptr || out_tokens == nullptr ||
+      out_num_accepted == nullptr)
+    return SPEC_ERR_INVALID_ARG;
+  if (int e = check_shape(B, gamma, V)) return e;
+  if (dt != SPEC_F32 && dt != SPEC_BF16) return SPEC_ERR_UNSUPPORTED;
+  if (!aligned16(target_logits) || !aligned16(draft_logits)) return SPEC_ERR_ALIGNMENT;
+  if (out_debug != nullptr && !aligned16(out_debug)) return SPEC_ERR_ALIGNMENT;
+  const Layout L = layout(B, gamma, V);
+  if (L.total > kNoAllocScratchBytes) return SPEC_ERR_WORKSPACE;  // beyond the built-in scratch
+  void* scratch = nullptr;
+  if (int e = noalloc_scratch(&scratch)) return e;
+  // the per-sequence counters must start at zero even if an earlier call was
+  // cut short; everything else in the scratch is written before it is read
+  if (cudaMemsetAsync(static_cast<unsigned char*>(scratch) + L.tail_done, 0, L.total - L.tail_done,
+                      static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+  return spec_verify_sample(target_logits, draft_logits, dt, draft_tokens, temperature, u_accept,
+                            u_resample, B, gamma, V, out_tokens, out_num_accepted, out_debug, scratch,
+                            kNoAllocScratchBytes, stream);
+}
