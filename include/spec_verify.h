@@ -59,9 +59,13 @@ enum {
 
 /*
  * Bytes of workspace needed for batches up to B sequences, draft length up to
- * gamma and vocabulary up to V (H = lm_head hidden size, 0 when the lm_head
- * entry point is not used).  Writes *bytes; returns SPEC_OK or
- * SPEC_ERR_INVALID_ARG.
+ * gamma and vocabulary up to V.  H = 0 sizes it for the logit entry points;
+ * H > 0 (the lm_head hidden size) for spec_verify_lmhead_sample, and that
+ * workspace serves the logit entry points too.  The lm_head size includes the
+ * stored fp32 target logits of rows j < gamma, B*gamma*V*4 bytes (268 MB at
+ * B=64, gamma=4, V=262144).  Writes *bytes; returns SPEC_OK,
+ * SPEC_ERR_INVALID_ARG, or SPEC_ERR_UNSUPPORTED for lm_head shapes beyond
+ * its limits (see spec_verify_lmhead_sample).
  */
 int spec_verify_workspace_bytes(int B, int gamma, int V, int H, size_t *bytes);
 
@@ -159,6 +163,48 @@ int spec_verify_sample_noalloc(const void *target_logits, const void *draft_logi
                                const float *u_resample, int B, int gamma, int V,
                                int32_t *out_tokens, int32_t *out_num_accepted,
                                float *out_debug, void *stream);
+
+/*
+ * Rejection-sampling verification with the target logits computed in the
+ * call: l[b, j, x] = sum_k hidden[b*(gamma+1)+j, k] * W[x, k], the target's
+ * final hidden states times its output embedding (tied to the input
+ * embedding: "Gemma 4 Multi-Token Prediction (MTP) 深度解析" §3.1; "Gemma 4 -
+ * Drafter 解析", 高效 Embedder).  The GEMM runs on the tcgen05 tensor cores
+ * (bf16 operands, fp32 accumulation) and the target logits are reduced to
+ * the verify statistics as they leave the accumulator; only rows j < gamma of
+ * sampling sequences are stored (fp32, in the workspace) because the residual
+ * max(0, p_n - q_n) needs them after the decision.  The rule, the uniforms and
+ * the outputs are those of spec_verify_sample.
+ *
+ *   hidden        [B*(gamma+1), H] bf16: rows b*(gamma+1) .. b*(gamma+1)+gamma
+ *                 are sequence b's verify positions 0..gamma
+ *   W             [V, H] bf16
+ *   draft_logits  [B, gamma, V] bf16
+ *   draft_tokens, temperature, u_accept, u_resample, out_*: as spec_verify_sample
+ *
+ * Limits: B*(gamma+1) <= 384 rows, H a multiple of 64 in [64, 65536], V a
+ * multiple of 8; hidden, W and draft_logits 16-byte aligned.  Beyond the row
+ * limit the call returns SPEC_ERR_UNSUPPORTED.  The workspace must come from
+ * spec_verify_workspace_bytes(B, gamma, V, H, ...).
+ */
+int spec_verify_lmhead_sample(const void *hidden, const void *W, const void *draft_logits,
+                              const int32_t *draft_tokens, const float *temperature,
+                              const float *u_accept, const float *u_resample, int B,
+                              int gamma, int V, int H, int32_t *out_tokens,
+                              int32_t *out_num_accepted, float *out_debug,
+                              void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Timing / profiling aid: the same arguments and checks as
+ * spec_verify_lmhead_sample, but only its lm_head GEMM kernel is enqueued, in
+ * the launch configuration that call uses.  Outputs are not written.
+ */
+int spec_verify_lmhead_gemm_only(const void *hidden, const void *W, const void *draft_logits,
+                                 const int32_t *draft_tokens, const float *temperature,
+                                 const float *u_accept, const float *u_resample, int B,
+                                 int gamma, int V, int H, int32_t *out_tokens,
+                                 int32_t *out_num_accepted, float *out_debug,
+                                 void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * Synchronise `stream`, then return the device-side status recorded in

@@ -295,10 +295,11 @@ def verify_lmhead_sample(hidden, W, draft, draft_tokens, temperature,
     B = len(draft_tokens)
     idx = range(B) if seqs is None else seqs
     h = _as_f64(hidden)
+    Wf = _as_f64(W)  # widened once for all sequences
     out = []
     for b in idx:
         rows = h[b * (gamma + 1):(b + 1) * (gamma + 1)]
-        tp = lmhead_logits(rows, W)
+        tp = lmhead_logits(rows, Wf)
         out.append(verify_sample_seq(tp, draft[b], draft_tokens[b],
                                      temperature[b], u_accept[b], u_resample[b]))
     return out

@@ -28,7 +28,7 @@ EXPORTED = (
     "spec_verify_workspace_bytes", "spec_verify_workspace_init", "spec_verify_greedy",
     "spec_verify_sample", "spec_verify_status", "spec_verify_error_string",
     "spec_verify_version", "spec_verify_selftest_timeout", "spec_verify_sample_reduce_only",
-    "spec_verify_sample_noalloc",
+    "spec_verify_sample_noalloc", "spec_verify_lmhead_sample", "spec_verify_lmhead_gemm_only",
 )
 
 
@@ -63,6 +63,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.spec_verify_sample_reduce_only.argtypes = list(lib.spec_verify_sample.argtypes)
     lib.spec_verify_sample_noalloc.argtypes = [_vp, _vp, _i, _vp, _vp, _vp, _vp, _i, _i, _i,
                                                _vp, _vp, _vp, _vp]
+    lib.spec_verify_lmhead_sample.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i,
+                                              _vp, _vp, _vp, _vp, _sz, _vp]
+    lib.spec_verify_lmhead_gemm_only.argtypes = list(lib.spec_verify_lmhead_sample.argtypes)
     lib.spec_verify_status.argtypes = [_vp, _vp]
     lib.spec_verify_error_string.argtypes = [_i]
     lib.spec_verify_error_string.restype = ctypes.c_char_p
@@ -198,6 +201,44 @@ def spec_verify_sample_noalloc(target_logits, draft_logits, draft_tokens, temper
         _ptr(target_logits), _ptr(draft_logits), _dtype_code(target_logits), _ptr(draft_tokens),
         _ptr(temperature), _ptr(u_accept), _ptr(u_resample), B, g1 - 1, V, _ptr(out_tokens),
         _ptr(out_num_accepted), _ptr(out_debug), _stream(stream)), "spec_verify_sample_noalloc")
+
+
+def _lmhead_call(fn, name, hidden, W, draft_logits, draft_tokens, temperature, u_accept,
+                 u_resample, out_tokens, out_num_accepted, workspace, out_debug, stream):
+    import torch
+    B, gamma, V = draft_logits.shape
+    H = W.shape[1]
+    for t, what in ((hidden, "hidden"), (W, "W"), (draft_logits, "draft_logits")):
+        if t.dtype != torch.bfloat16:
+            raise SpecVerifyError(SPEC_ERR_UNSUPPORTED, f"{what} must be bfloat16, got {t.dtype}")
+    if tuple(hidden.shape) != (B * (gamma + 1), H) or W.shape[0] != V:
+        raise SpecVerifyError(SPEC_ERR_INVALID_ARG, f"{name}: hidden {tuple(hidden.shape)}, "
+                              f"W {tuple(W.shape)}, draft_logits {tuple(draft_logits.shape)}")
+    _check(fn(_ptr(hidden), _ptr(W), _ptr(draft_logits), _ptr(draft_tokens), _ptr(temperature),
+              _ptr(u_accept), _ptr(u_resample), B, gamma, V, H, _ptr(out_tokens),
+              _ptr(out_num_accepted), _ptr(out_debug), _ptr(workspace), _nbytes(workspace),
+              _stream(stream)), name)
+
+
+def spec_verify_lmhead_sample(hidden, W, draft_logits, draft_tokens, temperature, u_accept,
+                              u_resample, out_tokens, out_num_accepted, workspace, out_debug=None,
+                              stream=None) -> None:
+    """Sampling verification with the target logits computed in the call as
+    hidden @ W^T: hidden [B*(gamma+1), H], W [V, H], draft_logits [B, gamma, V]
+    (all bfloat16); the other arguments as spec_verify_sample.  The workspace
+    comes from make_workspace(B, gamma, V, H)."""
+    _lmhead_call(load().spec_verify_lmhead_sample, "spec_verify_lmhead_sample", hidden, W,
+                 draft_logits, draft_tokens, temperature, u_accept, u_resample, out_tokens,
+                 out_num_accepted, workspace, out_debug, stream)
+
+
+def spec_verify_lmhead_gemm_only(hidden, W, draft_logits, draft_tokens, temperature, u_accept,
+                                 u_resample, out_tokens, out_num_accepted, workspace,
+                                 out_debug=None, stream=None) -> None:
+    """Enqueue only the lm_head GEMM kernel of spec_verify_lmhead_sample (timing aid)."""
+    _lmhead_call(load().spec_verify_lmhead_gemm_only, "spec_verify_lmhead_gemm_only", hidden, W,
+                 draft_logits, draft_tokens, temperature, u_accept, u_resample, out_tokens,
+                 out_num_accepted, workspace, out_debug, stream)
 
 
 def spec_verify_status(workspace, stream=None) -> int:

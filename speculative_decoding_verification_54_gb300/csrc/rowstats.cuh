@@ -52,14 +52,15 @@ struct RowStatsParams {
   float4* partials;          // [B*(2*gamma+1)*cpr] {M, s, argmax bits, mk}
   int* status;
   int B, gamma, V, CE, cpr;
-  int debug;  // bit 0: forced-timeout self-test
+  int draft_only;  // skip the target rows (their statistics come from the lm_head epilogue)
+  int debug;       // bit 0: forced-timeout self-test
 };
 
 // Row slot t of sequence b: t <= gamma is target row t, t > gamma is draft row
 // t-gamma-1.
 __device__ __forceinline__ int row_mode(const RowStatsParams& p, int b, int t) {
   const bool greedy = (p.draft == nullptr) || seq_is_greedy(p.temperature, b);
-  if (t <= p.gamma) return greedy ? kRowArgmax : kRowFull;
+  if (t <= p.gamma) return p.draft_only ? kRowSkip : (greedy ? kRowArgmax : kRowFull);
   return greedy ? kRowSkip : kRowFull;
 }
 

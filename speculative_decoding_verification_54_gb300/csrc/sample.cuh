@@ -16,8 +16,8 @@
 // that CTA) draws the token by inverse CDF in ascending vocabulary order, the
 // smallest k with sum_{x<=k} w(x) > u*Z: one warp scans the chunk masses to
 // pick the chunk, then scans that chunk's entries.  Element weights are fp32;
-// running sums across lanes and chunks are fp64, a few dozen operations per
-// lane since FP64 is slow on GB300.
+// running sums across lanes and chunks are two-float (F2) sums, since FP64 is
+// slow on GB300.
 #pragma once
 
 #include <cfloat>
@@ -145,6 +145,85 @@ __device__ __forceinline__ float chunk_mass(const SampleParams& p, const WeightF
   return warp_sum(acc);
 }
 
+// Level 1 of the inverse-CDF draw, warp-wide.  Lane l owns the contiguous
+// chunk range [c0, c1) of the chunk masses; the scan gives each lane its own
+// sum and the inclusive sum over lanes, and Z the total.
+struct MassScan {
+  F2 lsum, incl, Z;
+  int c0, c1;
+};
+__device__ __forceinline__ MassScan scan_masses(const float* mass, int n) {
+  const int lane = threadIdx.x & 31;
+  const int per = (n + 31) / 32;
+  MassScan ms;
+  ms.c0 = min(n, lane * per);
+  ms.c1 = min(n, ms.c0 + per);
+  ms.lsum = f2_from(0.f);
+#pragma unroll 4
+  for (int c = ms.c0; c < ms.c1; ++c) ms.lsum = f2_add(ms.lsum, f2_from(__ldcg(mass + c)));
+  ms.incl = warp_scan_incl(ms.lsum);
+  ms.Z = f2_shfl(ms.incl, 31);
+  return ms;
+}
+
+// The chunk holding `target` (= u*Z): the smallest c whose inclusive prefix
+// exceeds it.  *local receives target minus the mass before that chunk, or
+// FLT_MAX when rounding puts the target at or beyond the total, in which case
+// the last chunk of nonzero mass is taken.
+__device__ __forceinline__ int pick_chunk(const float* mass, const MassScan& ms, F2 target, F2* local) {
+  const int lane = threadIdx.x & 31;
+  const unsigned over = __ballot_sync(0xffffffffu, f2_gt(ms.incl, target));
+  int chunk = -1;
+  F2 loc = F2{FLT_MAX, 0.f};
+  if (over) {
+    const int L = __ffs(over) - 1;
+    if (lane == L) {
+      F2 run = f2_sub(ms.incl, ms.lsum);
+      for (int c = ms.c0; c < ms.c1; ++c) {
+        const F2 nxt = f2_add(run, f2_from(__ldcg(mass + c)));
+        if (f2_gt(nxt, target)) {
+          chunk = c;
+          loc = f2_sub(target, run);
+          break;
+        }
+        run = nxt;
+      }
+      if (chunk < 0) {  // rounding inside the lane: its last nonzero chunk
+        for (int c = ms.c1 - 1; c >= ms.c0; --c)
+          if (__ldcg(mass + c) > 0.f) {
+            chunk = c;
+            break;
+          }
+      }
+    }
+    chunk = __shfl_sync(0xffffffffu, chunk, L);
+    loc = f2_shfl(loc, L);
+  }
+  if (chunk < 0) {  // u*Z at or beyond the total: the last nonzero chunk
+    int last = -1;
+    for (int c = ms.c0; c < ms.c1; ++c)
+      if (__ldcg(mass + c) > 0.f) last = c;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, off));
+    chunk = last < 0 ? 0 : last;
+    loc = F2{FLT_MAX, 0.f};
+  }
+  *local = loc;
+  return chunk;
+}
+
+// Chunk masses of a plain row from its partials {M, s, argmax, mk}, in units
+// of 2^mk (mk: the row's combined scaled max); this lane's range [c0, c1).
+__device__ __forceinline__ void masses_from_partials(const float4* P, float mk, float* mass, int n) {
+  const int lane = threadIdx.x & 31;
+  const int per = (n + 31) / 32;
+  const int c0 = min(n, lane * per), c1 = min(n, c0 + per);
+  for (int c = c0; c < c1; ++c) {
+    const float4 q = __ldcg(P + c);
+    mass[c] = q.y * ex2(q.w - mk);
+  }
+}
+
 // The inverse-CDF draw for sequence b (warp-wide, one warp of the last CTA).
 // rs: the sequence's combined rows; s: its decision.
 template <typename T>
@@ -154,69 +233,20 @@ __device__ __noinline__ void draw_token(const SampleParams& p, int b, const SeqS
   const int lane = threadIdx.x & 31;
   const int g = p.gamma, slots = 2 * g + 1;
   float* mass = p.mass + static_cast<size_t>(b) * p.cpr;
-  const int per = (p.cpr + 31) / 32;
-  const int c0 = min(p.cpr, lane * per), c1 = min(p.cpr, c0 + per);
   bool residual = (s.mode == kModeResidual);
   const int rowp = residual ? s.n : g;
 
-  // ---- level 1: which chunk (lane-contiguous chunk ranges) ----
-  F2 lsum = f2_from(0.f);
-#pragma unroll 4
-  for (int c = c0; c < c1; ++c) lsum = f2_add(lsum, f2_from(__ldcg(mass + c)));
-  F2 incl = warp_scan_incl(lsum);
-  F2 Z = f2_shfl(incl, 31);
-  if (residual && !(Z.hi > 0.f)) {
+  // ---- level 1: which chunk ----
+  MassScan ms = scan_masses(mass, p.cpr);
+  if (residual && !(ms.Z.hi > 0.f)) {
     // Z == 0 cannot happen in exact arithmetic; if rounding produces it, draw
     // from p_n itself (chunk masses from the row partials)
-    const float4* P4 = p.partials + static_cast<size_t>(b * slots + s.n) * p.cpr;
-    const float mk = rs[s.n].mk;
-    lsum = f2_from(0.f);
-    for (int c = c0; c < c1; ++c) {
-      const float4 q = __ldcg(P4 + c);
-      mass[c] = q.y * ex2(q.w - mk);
-      lsum = f2_add(lsum, f2_from(mass[c]));
-    }
-    incl = warp_scan_incl(lsum);
-    Z = f2_shfl(incl, 31);
+    masses_from_partials(p.partials + static_cast<size_t>(b * slots + s.n) * p.cpr, rs[s.n].mk, mass, p.cpr);
+    ms = scan_masses(mass, p.cpr);
     residual = false;  // weights of target row n as a plain row
   }
-  const F2 target = f2_mul_f(Z, p.u_resample[b]);
-  const unsigned over = __ballot_sync(0xffffffffu, f2_gt(incl, target));
-  int chunk = -1;
-  F2 local = F2{FLT_MAX, 0.f};
-  if (over) {
-    const int L = __ffs(over) - 1;
-    if (lane == L) {
-      F2 run = f2_sub(incl, lsum);
-      for (int c = c0; c < c1; ++c) {
-        const F2 nxt = f2_add(run, f2_from(__ldcg(mass + c)));
-        if (f2_gt(nxt, target)) {
-          chunk = c;
-          local = f2_sub(target, run);
-          break;
-        }
-        run = nxt;
-      }
-      if (chunk < 0) {  // rounding inside the lane: its last nonzero chunk
-        for (int c = c1 - 1; c >= c0; --c)
-          if (__ldcg(mass + c) > 0.f) {
-            chunk = c;
-            break;
-          }
-      }
-    }
-    chunk = __shfl_sync(0xffffffffu, chunk, L);
-    local = f2_shfl(local, L);
-  }
-  if (chunk < 0) {  // u*Z at or beyond the total: the last nonzero chunk
-    int last = -1;
-    for (int c = c0; c < c1; ++c)
-      if (__ldcg(mass + c) > 0.f) last = c;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, off));
-    chunk = last < 0 ? 0 : last;
-    local = F2{FLT_MAX, 0.f};
-  }
+  F2 local;
+  const int chunk = pick_chunk(mass, ms, f2_mul_f(ms.Z, p.u_resample[b]), &local);
 
   // ---- level 2: which entry inside the chunk.  The chunk's 256 vectors are
   // taken in two halves; in each, lane l holds the contiguous vectors

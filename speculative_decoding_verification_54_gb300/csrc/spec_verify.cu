@@ -9,16 +9,25 @@
 // The tail kernel is launched with programmatic stream serialization so its
 // launch latency overlaps the row reducer; it waits for the reducer's results
 // with griddepcontrol.wait before reading them.
+//
+// With the fused lm_head (spec_verify_lmhead_sample) the chain is
+//   rowstats (draft rows only) -> lmhead (tcgen05 GEMM + statistics epilogue)
+//   -> lm_decide -> lm_tail,
+// every launch after the first with programmatic stream serialization.
+#include <cuda.h>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
 
-#include "decide.cuh"
 #include "common.cuh"
+#include "decide.cuh"
+#include "lmhead.cuh"
+#include "lmtail.cuh"
 #include "rowstats.cuh"
 #include "sample.cuh"
 #include "spec_verify.h"
+#include "tc.cuh"
 
 using namespace specv;
 
@@ -47,7 +56,9 @@ int device_info(DeviceInfo* out) {
     if (cudaFuncSetAttribute(rowstats_kernel<float, kTma>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smem) != cudaSuccess ||
         cudaFuncSetAttribute(rowstats_kernel<__nv_bfloat16, kTma>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
+        cudaFuncSetAttribute(lmhead_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kLmSmemBytes)) != cudaSuccess)
       return SPEC_ERR_CUDA;
     const char* env = std::getenv("SPECV_ROW_LOADS");
     d.path = (env != nullptr && std::strcmp(env, "tma") == 0) ? kTma : kLdg;
@@ -97,9 +108,8 @@ struct Plan {
   size_t smem;
 };
 
-Plan make_plan(int B, int gamma, int V, size_t esize, int sms, bool sampling, int path) {
+Plan make_plan_rows(int rows, int V, size_t esize, int sms, int path) {
   Plan p;
-  const int rows = B * (sampling ? (2 * gamma + 1) : (gamma + 1));
   int CE = static_cast<int>(kChunkBytes / esize);
   while (CE > kMinChunk && static_cast<long long>(rows) * ((V + CE - 1) / CE) < 8LL * sms) CE >>= 1;
   p.CE = CE;
@@ -111,6 +121,10 @@ Plan make_plan(int B, int gamma, int V, size_t esize, int sms, bool sampling, in
   if (p.grid < 1) p.grid = 1;
   p.smem = (path == kTma) ? kTmaRingBytes : 0;
   return p;
+}
+
+Plan make_plan(int B, int gamma, int V, size_t esize, int sms, bool sampling, int path) {
+  return make_plan_rows(B * (sampling ? (2 * gamma + 1) : (gamma + 1)), V, esize, sms, path);
 }
 
 template <typename Kern, typename Params>
@@ -157,7 +171,7 @@ int run_chain(const Common& a, bool sampling) {
   int* status = reinterpret_cast<int*>(ws + L.header);
   const Plan pl = make_plan(a.B, a.gamma, a.V, sizeof(T), dev.sms, sampling, dev.path);
 
-  RowStatsParams rp;
+  RowStatsParams rp = {};
   rp.target = a.target;
   rp.draft = sampling ? a.draft : nullptr;
   rp.temperature = sampling ? a.temperature : nullptr;
@@ -217,11 +231,194 @@ int dispatch(const Common& a, bool sampling) {
   return SPEC_ERR_UNSUPPORTED;
 }
 
+// ---------------------------------------------------------------------------
+// fused lm_head chain
+// ---------------------------------------------------------------------------
+constexpr int kLmMaxRows = kLmMaxMTiles * kLmTileM;  // 384 verify rows per call
+
+struct LmLayout {
+  Layout base;  // header, draft-row partials, counters
+  size_t tpart, logits, rowstat, seq, mass, total;
+  int n_tiles;
+};
+
+LmLayout lm_layout(int B, int gamma, int V) {
+  LmLayout L;
+  L.base = layout(B, gamma, V);
+  L.n_tiles = (V + kLmTileN - 1) / kLmTileN;
+  const size_t R = static_cast<size_t>(B) * (gamma + 1);
+  size_t off = L.base.total;
+  L.tpart = off;
+  off += align_up(R * L.n_tiles * sizeof(float4), 256);
+  L.logits = off;
+  off += align_up(static_cast<size_t>(B) * gamma * V * sizeof(float), 256);
+  L.rowstat = off;
+  off += align_up(static_cast<size_t>(B) * (2 * gamma + 1) * sizeof(RowStat), 256);
+  L.seq = off;
+  off += align_up(static_cast<size_t>(B) * sizeof(SeqState), 256);
+  L.mass = off;
+  off += align_up(static_cast<size_t>(B) * L.n_tiles * sizeof(float), 256);
+  L.total = off;
+  return L;
+}
+
+int check_lm_shape(int B, int gamma, int V, int H) {
+  if (int e = check_shape(B, gamma, V)) return e;
+  if (H < kLmTileK || H > 65536 || (H % kLmTileK) != 0) return SPEC_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * (gamma + 1) > kLmMaxRows) return SPEC_ERR_UNSUPPORTED;
+  return SPEC_OK;
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+std::mutex g_encode_mu;
+
+EncodeTiledFn encoder() {
+  std::lock_guard<std::mutex> lk(g_encode_mu);
+  if (g_encode == nullptr) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  }
+  return g_encode;
+}
+
+// 2-D bf16 tensor map over a [rows, H] row-major matrix: boxes of 64 x 128
+// (128-byte rows, swizzled as the tcgen05 descriptors expect); rows past the
+// end read as zero.
+bool encode_rows(CUtensorMap* m, const void* base, int rows, int H) {
+  EncodeTiledFn enc = encoder();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(H) * 2};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kLmTileK), static_cast<cuuint32_t>(kLmTileM)};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct LmArgs {
+  const void* hidden;
+  const void* W;
+  const void* draft;
+  const int32_t* draft_tokens;
+  const float* temperature;
+  const float* u_accept;
+  const float* u_resample;
+  int B, gamma, V, H;
+  int32_t* out_tokens;
+  int32_t* out_num;
+  float* out_debug;
+  void* ws;
+  size_t ws_bytes;
+  cudaStream_t stream;
+  bool gemm_only;  // launch only the lm_head kernel (timing / profiling)
+};
+
+int run_lm_chain(const LmArgs& a) {
+  const LmLayout L = lm_layout(a.B, a.gamma, a.V);
+  if (a.ws_bytes < L.total) return SPEC_ERR_WORKSPACE;
+  DeviceInfo dev;
+  if (device_info(&dev) != SPEC_OK) return SPEC_ERR_CUDA;
+  uint8_t* ws = static_cast<uint8_t*>(a.ws);
+  int* status = reinterpret_cast<int*>(ws + L.base.header);
+  const int R = a.B * (a.gamma + 1);
+
+  // 1. draft rows: chunk partials (the row reducer, target rows skipped)
+  const Plan pl = make_plan_rows(a.B * a.gamma, a.V, sizeof(__nv_bfloat16), dev.sms, kLdg);
+  RowStatsParams rp = {};
+  rp.target = nullptr;
+  rp.draft = a.draft;
+  rp.temperature = a.temperature;
+  rp.partials = reinterpret_cast<float4*>(ws + L.base.partials);
+  rp.status = status;
+  rp.B = a.B;
+  rp.gamma = a.gamma;
+  rp.V = a.V;
+  rp.CE = pl.CE;
+  rp.cpr = pl.cpr;
+  rp.draft_only = 1;
+  if (!a.gemm_only) {
+    rowstats_kernel<__nv_bfloat16, kLdg><<<pl.grid, kRowThreads, 0, a.stream>>>(rp);
+    if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
+  }
+
+  // 2. target rows: the lm_head GEMM with its statistics epilogue
+  LmParams lp;
+  std::memset(&lp, 0, sizeof(lp));
+  if (!encode_rows(&lp.tmA, a.hidden, R, a.H) || !encode_rows(&lp.tmB, a.W, a.V, a.H)) return SPEC_ERR_CUDA;
+  lp.R = R;
+  lp.n_mtiles = (R + kLmTileM - 1) / kLmTileM;
+  lp.V = a.V;
+  lp.H = a.H;
+  lp.n_tiles = L.n_tiles;
+  lp.gamma = a.gamma;
+  lp.temperature = a.temperature;
+  lp.partials = reinterpret_cast<float4*>(ws + L.tpart);
+  lp.logits = reinterpret_cast<float*>(ws + L.logits);
+  lp.status = status;
+  const int lm_grid = L.n_tiles < dev.sms ? L.n_tiles : dev.sms;
+  if (a.gemm_only) {  // first kernel of the call: plain stream order
+    lmhead_kernel<<<lm_grid, kLmThreads, kLmSmemBytes, a.stream>>>(lp);
+    return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+  }
+  if (launch_pdl(lmhead_kernel, dim3(lm_grid), dim3(kLmThreads), kLmSmemBytes, a.stream, lp) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+
+  // 3. decision, 4. residual / bonus masses and the draw
+  LmTailParams tp = {};
+  tp.hidden = static_cast<const __nv_bfloat16*>(a.hidden);
+  tp.W = static_cast<const __nv_bfloat16*>(a.W);
+  tp.draft = static_cast<const __nv_bfloat16*>(a.draft);
+  tp.logits = lp.logits;
+  tp.tpart = lp.partials;
+  tp.dpart = rp.partials;
+  tp.rowstat = reinterpret_cast<RowStat*>(ws + L.rowstat);
+  tp.seq = reinterpret_cast<SeqState*>(ws + L.seq);
+  tp.mass = reinterpret_cast<float*>(ws + L.mass);
+  tp.tail_done = reinterpret_cast<int*>(ws + L.base.tail_done);
+  tp.u_resample = a.u_resample;
+  tp.B = a.B;
+  tp.gamma = a.gamma;
+  tp.V = a.V;
+  tp.H = a.H;
+  tp.n_tiles = L.n_tiles;
+  tp.cpr_d = pl.cpr;
+  DecideParams& dp = tp.dp;
+  dp.target = nullptr;
+  dp.draft = a.draft;
+  dp.draft_tokens = a.draft_tokens;
+  dp.temperature = a.temperature;
+  dp.u_accept = a.u_accept;
+  dp.out_tokens = a.out_tokens;
+  dp.out_num = a.out_num;
+  dp.out_debug = a.out_debug;
+  dp.status = status;
+  dp.gamma = a.gamma;
+  dp.V = a.V;
+  if (launch_pdl(lm_decide_kernel, dim3(a.B), dim3(kLmTailThreads), 0, a.stream, tp) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+  // parts per sequence: about three CTAs per SM over the batch, >= 8 tiles each
+  int parts = (3 * dev.sms + a.B - 1) / a.B;
+  if (parts > L.n_tiles / 8) parts = L.n_tiles / 8;
+  if (parts > 64) parts = 64;
+  if (parts < 1) parts = 1;
+  if (launch_pdl(lm_tail_kernel, dim3(parts, a.B), dim3(kLmTailThreads), 0, a.stream, tp) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+  return SPEC_OK;
+}
+
 }  // namespace
 
 extern "C" {
 
-int spec_verify_version(void) { return 100; }
+int spec_verify_version(void) { return 200; }
 
 const char* spec_verify_error_string(int code) {
   switch (code) {
@@ -239,8 +436,13 @@ const char* spec_verify_error_string(int code) {
 
 int spec_verify_workspace_bytes(int B, int gamma, int V, int H, size_t* bytes) {
   if (bytes == nullptr) return SPEC_ERR_INVALID_ARG;
-  if (check_shape(B, gamma, V) != SPEC_OK || H < 0) return SPEC_ERR_INVALID_ARG;
-  *bytes = layout(B, gamma, V).total;
+  if (H == 0) {
+    if (check_shape(B, gamma, V) != SPEC_OK) return SPEC_ERR_INVALID_ARG;
+    *bytes = layout(B, gamma, V).total;
+    return SPEC_OK;
+  }
+  if (int e = check_lm_shape(B, gamma, V, H)) return e;
+  *bytes = lm_layout(B, gamma, V).total;
   return SPEC_OK;
 }
 
@@ -332,6 +534,60 @@ int spec_verify_sample_reduce_only(const void* target_logits, const void* draft_
   return sample_entry(true, target_logits, draft_logits, dt, draft_tokens, temperature, u_accept,
                       u_resample, B, gamma, V, out_tokens, out_num_accepted, out_debug, workspace,
                       workspace_bytes, stream);
+}
+
+static int lmhead_entry(bool gemm_only, const void* hidden, const void* W, const void* draft_logits,
+                        const int32_t* draft_tokens, const float* temperature, const float* u_accept,
+                        const float* u_resample, int B, int gamma, int V, int H, int32_t* out_tokens,
+                        int32_t* out_num_accepted, float* out_debug, void* workspace, size_t workspace_bytes,
+                        void* stream) {
+  if (hidden == nullptr || W == nullptr || draft_logits == nullptr || draft_tokens == nullptr ||
+      temperature == nullptr || u_accept == nullptr || u_resample == nullptr || out_tokens == nullptr ||
+      out_num_accepted == nullptr)
+    return SPEC_ERR_INVALID_ARG;
+  if (int e = check_lm_shape(B, gamma, V, H)) return e;
+  if (!aligned16(hidden) || !aligned16(W) || !aligned16(draft_logits)) return SPEC_ERR_ALIGNMENT;
+  if (out_debug != nullptr && !aligned16(out_debug)) return SPEC_ERR_ALIGNMENT;
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return SPEC_ERR_WORKSPACE;
+  LmArgs a = {};
+  a.hidden = hidden;
+  a.W = W;
+  a.draft = draft_logits;
+  a.draft_tokens = draft_tokens;
+  a.temperature = temperature;
+  a.u_accept = u_accept;
+  a.u_resample = u_resample;
+  a.B = B;
+  a.gamma = gamma;
+  a.V = V;
+  a.H = H;
+  a.out_tokens = out_tokens;
+  a.out_num = out_num_accepted;
+  a.out_debug = out_debug;
+  a.ws = workspace;
+  a.ws_bytes = workspace_bytes;
+  a.stream = static_cast<cudaStream_t>(stream);
+  a.gemm_only = gemm_only;
+  return run_lm_chain(a);
+}
+
+int spec_verify_lmhead_sample(const void* hidden, const void* W, const void* draft_logits,
+                              const int32_t* draft_tokens, const float* temperature, const float* u_accept,
+                              const float* u_resample, int B, int gamma, int V, int H, int32_t* out_tokens,
+                              int32_t* out_num_accepted, float* out_debug, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  return lmhead_entry(false, hidden, W, draft_logits, draft_tokens, temperature, u_accept, u_resample, B, gamma,
+                      V, H, out_tokens, out_num_accepted, out_debug, workspace, workspace_bytes, stream);
+}
+
+int spec_verify_lmhead_gemm_only(const void* hidden, const void* W, const void* draft_logits,
+                                 const int32_t* draft_tokens, const float* temperature, const float* u_accept,
+                                 const float* u_resample, int B, int gamma, int V, int H, int32_t* out_tokens,
+                                 int32_t* out_num_accepted, float* out_debug, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+  return lmhead_entry(true, hidden, W, draft_logits, draft_tokens, temperature, u_accept, u_resample, B, gamma,
+                      V, H, out_tokens, out_num_accepted, out_debug, workspace, workspace_bytes, stream);
 }
 
 int spec_verify_status(void* workspace, void* stream) {

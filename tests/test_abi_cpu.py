@@ -127,3 +127,50 @@ def test_binding_fails_loudly_without_library(tmp_path):
             binding.load(str(tmp_path / "missing.so"))
     finally:
         binding._lib = saved
+
+
+def _lmhead(lib, **kw):
+    args = dict(h=A16, w=A16, d=A16, tok=A16, temp=A16, ua=A16, ur=A16, B=64, g=4, V=262144,
+                H=1536, out=A16, num=A16, dbg=None, ws=WS, wsb=1 << 20)
+    args.update(kw)
+    return lib.spec_verify_lmhead_sample(args["h"], args["w"], args["d"], args["tok"], args["temp"],
+                                         args["ua"], args["ur"], args["B"], args["g"], args["V"],
+                                         args["H"], args["out"], args["num"], args["dbg"], args["ws"],
+                                         args["wsb"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(h=None), sv.SPEC_ERR_INVALID_ARG),
+    (dict(w=None), sv.SPEC_ERR_INVALID_ARG),
+    (dict(d=None), sv.SPEC_ERR_INVALID_ARG),
+    (dict(tok=None), sv.SPEC_ERR_INVALID_ARG),
+    (dict(ur=None), sv.SPEC_ERR_INVALID_ARG),
+    (dict(H=0), sv.SPEC_ERR_INVALID_ARG),
+    (dict(H=1000), sv.SPEC_ERR_INVALID_ARG),
+    (dict(V=262148), sv.SPEC_ERR_INVALID_ARG),
+    (dict(g=0), sv.SPEC_ERR_INVALID_ARG),
+    (dict(B=77), sv.SPEC_ERR_UNSUPPORTED),   # 77*5 = 385 verify rows > 384
+    (dict(B=13, g=31), sv.SPEC_ERR_UNSUPPORTED),  # 13*32 = 416 rows
+    (dict(h=A8), sv.SPEC_ERR_ALIGNMENT),
+    (dict(w=A8), sv.SPEC_ERR_ALIGNMENT),
+    (dict(d=A8), sv.SPEC_ERR_ALIGNMENT),
+    (dict(dbg=A8), sv.SPEC_ERR_ALIGNMENT),
+    (dict(ws=None), sv.SPEC_ERR_WORKSPACE),
+    (dict(ws=WS + 64), sv.SPEC_ERR_WORKSPACE),
+    (dict(wsb=1 << 20), sv.SPEC_ERR_WORKSPACE),  # the stored logits alone are 268 MB
+])
+def test_lmhead_rejects_bad_arguments_on_host(lib, kw, code):
+    assert _lmhead(lib, **kw) == code
+
+
+def test_lmhead_workspace_bytes(lib):
+    plain = sv.spec_verify_workspace_bytes(64, 4, 262144)
+    lm = sv.spec_verify_workspace_bytes(64, 4, 262144, 1536)
+    # the lm_head workspace holds the plain one plus the stored fp32 rows j < gamma
+    assert lm >= plain + 64 * 4 * 262144 * 4
+    assert lm % 256 == 0
+    for bad, code in (((64, 4, 262144, 100), sv.SPEC_ERR_INVALID_ARG),
+                      ((80, 4, 262144, 1536), sv.SPEC_ERR_UNSUPPORTED)):
+        with pytest.raises(sv.SpecVerifyError) as e:
+            sv.spec_verify_workspace_bytes(*bad)
+        assert e.value.code == code

@@ -1,0 +1,236 @@
+"""GPU (C ABI) vs fp64 oracle for the fused lm_head verify
+(spec_verify_lmhead_sample): target logits = hidden @ W^T on the tensor cores.
+
+Two kinds of inputs:
+* exact-sums recipe (hidden on a 1/8 grid, W on a 2^-11 grid): every logit is
+  exact in fp32 whatever the summation order, so the GPU's logits equal the
+  oracle's and the verify outputs are held to the same bar as the logit entry
+  points (exact, except uniforms within 1e-6 of a boundary; probabilities
+  within 1e-5);
+* the N(0,1) x N(0, 0.02^2) recipe: the GEMM's fp32 accumulation rounds, so
+  results are checked against the envelope that rounding allows (see
+  ``_check_envelope``).
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads as wl
+from tests.gpu_util import Tally, assert_tally, compare
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def sv():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from speculative_decoding_verification_54_gb300 import _build
+    _build.build()
+    import speculative_decoding_verification_54_gb300 as m
+    m.load()
+    torch.cuda.set_device(0)
+    return m
+
+
+@pytest.fixture(scope="module")
+def dev(sv):
+    import torch
+    return torch.device("cuda:0")
+
+
+def _bf16(a, dev):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+
+def to_device_lm(inp, dev, W=None):
+    import torch
+    f = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+    return dict(hidden=_bf16(inp.hidden, dev), W=W if W is not None else _bf16(inp.W, dev),
+                draft=_bf16(inp.draft, dev), draft_tokens=f(inp.draft_tokens),
+                temperature=f(inp.temperature), u_accept=f(inp.u_accept),
+                u_resample=f(inp.u_resample))
+
+
+def run_lm(sv, d, ws, debug=True):
+    import torch
+    B, gamma, V = d["draft"].shape
+    out = torch.full((B, gamma + 1), -7, dtype=torch.int32, device=d["draft"].device)
+    num = torch.full((B,), -7, dtype=torch.int32, device=d["draft"].device)
+    dbg = torch.zeros((B, gamma + 1, 4), dtype=torch.float32, device=d["draft"].device) if debug else None
+    sv.spec_verify_lmhead_sample(d["hidden"], d["W"], d["draft"], d["draft_tokens"], d["temperature"],
+                                 d["u_accept"], d["u_resample"], out, num, ws, out_debug=dbg)
+    st = sv.spec_verify_status(ws)
+    return out.cpu().numpy(), num.cpu().numpy(), (dbg.cpu().numpy() if debug else None), st
+
+
+def _oracle(inp, seqs=None):
+    return oracle.verify_lmhead_sample(inp.hidden, inp.W, inp.draft, inp.draft_tokens, inp.temperature,
+                                       inp.u_accept, inp.u_resample, inp.gamma, seqs=seqs)
+
+
+def _exact_case(sv, dev, B, gamma, V, H, rounds, temperature=None, seqs=None, label=""):
+    W = wl.make_lmhead_W(V, H, seed=0, exact_sums=True)
+    Wd = _bf16(W, dev)
+    ws = sv.make_workspace(B, gamma, V, H)
+    tally = Tally()
+    ns = []
+    for r in range(rounds):
+        inp = wl.make_lmhead_round(r, B=B, gamma=gamma, V=V, H=H, W_bits=W, exact_sums=True,
+                                   temperature=temperature)
+        tok, num, dbg, st = run_lm(sv, to_device_lm(inp, dev, Wd), ws)
+        assert st == sv.SPEC_OK
+        if seqs is None:
+            t = compare(_oracle(inp), tok, num, dbg, label=f"{label} round{r}")
+        else:
+            t = compare(_oracle(inp, seqs), tok, num, dbg, seqs=seqs, label=f"{label} round{r}")
+        tally.merge(t)
+        ns += [int(num[b]) for b in (seqs if seqs is not None else range(B))]
+    return tally, ns
+
+
+# ---------------------------------------------------------------------------
+# exact-sums recipe: the full parity bar
+# ---------------------------------------------------------------------------
+def test_lmhead_small_ragged_vocab(sv, dev):
+    """One M-tile (20 rows), a ragged last vocabulary tile (V = 37*128 + 8),
+    H = 256 (four K steps), 40 rounds."""
+    tally, ns = _exact_case(sv, dev, B=4, gamma=4, V=37 * 128 + 8, H=256, rounds=40, label="small")
+    assert_tally(tally)
+    assert min(ns) < 4 and max(ns) == 4  # rejections and fully accepted rounds (bonus)
+    print(f"lmhead small: {tally.exact} exact, {tally.excused} excused of {tally.checked}")
+
+
+def test_lmhead_three_mtiles_several_tiles_per_cta(sv, dev):
+    """R = 320 rows (three M-tiles, the last partly empty), V = 320 tiles so
+    each CTA runs two or three vocabulary tiles through one accumulator, and
+    H = 1536 (24 K steps around the 3-stage ring)."""
+    tally, ns = _exact_case(sv, dev, B=64, gamma=4, V=320 * 128, H=1536, rounds=2, label="3m")
+    assert_tally(tally)
+    assert tally.checked == 128
+    print(f"lmhead 3 M-tiles: {tally.exact} exact, {tally.excused} excused; n histogram "
+          f"{np.bincount(ns, minlength=5).tolist()}")
+
+
+def test_lmhead_mixed_greedy_and_sampling(sv, dev):
+    """Even sequences greedy (T = 0), odd ones sample at T = 1; gamma = 7."""
+    tally, ns = _exact_case(sv, dev, B=6, gamma=7, V=64 * 128, H=512, rounds=20,
+                            temperature=("alternate", 0.0, 1.0), label="mixed")
+    assert_tally(tally)
+
+
+def test_lmhead_all_greedy(sv, dev):
+    tally, _ = _exact_case(sv, dev, B=5, gamma=3, V=50 * 128, H=128, rounds=10, temperature=0.0,
+                           label="greedy")
+    assert_tally(tally)
+
+
+def test_lmhead_full_size_sampled_sequences(sv, dev):
+    """The fused workload's shape (B=64, gamma=4, V=262144, H=1536) on the
+    exact-sums recipe; the oracle checks 8 sequences spread over the batch
+    (each needs a 5 x 1536 x 262144 float64 product)."""
+    seqs = [0, 9, 18, 27, 36, 45, 54, 63]
+    tally, _ = _exact_case(sv, dev, B=64, gamma=4, V=262144, H=1536, rounds=1, seqs=seqs,
+                           label="full")
+    assert_tally(tally)
+
+
+def test_lmhead_workspace_reuse_and_determinism(sv, dev):
+    B, gamma, V, H = 8, 4, 96 * 128, 256
+    W = wl.make_lmhead_W(V, H, seed=0, exact_sums=True)
+    inp = wl.make_lmhead_round(3, B=B, gamma=gamma, V=V, H=H, W_bits=W, exact_sums=True)
+    ws = sv.make_workspace(B, gamma, V, H)
+    d = to_device_lm(inp, dev)
+    first = run_lm(sv, d, ws)
+    for _ in range(3):
+        again = run_lm(sv, d, ws)
+        assert np.array_equal(first[0], again[0]) and np.array_equal(first[1], again[1])
+        assert np.array_equal(first[2], again[2], equal_nan=True)
+
+
+# ---------------------------------------------------------------------------
+# the N(0,1) x N(0, 0.02^2) recipe: within the fp32 accumulation envelope
+# ---------------------------------------------------------------------------
+def _logit_error_bound(hidden_f64, W_f64, rows):
+    """Deterministic bound on |fl32(sum_k h_k w_k) - sum_k h_k w_k| for any
+    summation order of H exact products: gamma_{H-1} * sum_k |h_k w_k|
+    (gamma_n = n u / (1 - n u), u = 2^-24), maximised over the vocabulary."""
+    H = hidden_f64.shape[1]
+    u = 2.0 ** -24
+    gam = (H - 1) * u / (1 - (H - 1) * u)
+    return gam * (np.abs(hidden_f64[rows]) @ np.abs(W_f64).T).max(axis=1)
+
+
+def _check_envelope(res, b, inp, tok, num, dbg, eps_rows):
+    """The GPU result for sequence b must be one the oracle gives for some
+    target logits within eps of the exact ones.  eps shifts each log p_j by
+    at most 2*eps/T, so: every decision whose ratio rho is farther than that
+    (relative) from u must agree; L_p within eps/T; and the emitted token's
+    oracle CDF interval must come within delta of u, delta bounding how far
+    such a perturbation moves the normalised CDF."""
+    T = float(inp.temperature[b])
+    g = inp.gamma
+    eps = float(max(eps_rows))
+    k = 2 * eps / T
+    # normalisers
+    for j in range(g + 1):
+        assert abs(dbg[b, j, 2] - res.L_p[j]) <= eps / T + 1e-5 * max(1.0, abs(res.L_p[j]))
+    n_gpu = int(num[b])
+    # decisions before min(n_gpu, n_oracle) were accepted on both sides; the
+    # first one on which they differ must lie within the envelope
+    if n_gpu != res.n:
+        j = min(n_gpu, res.n)
+        rho = res.p_tok[j] / res.q_tok[j] if res.q_tok[j] > 0 else math.inf
+        u = float(inp.u_accept[b, j])
+        assert abs(u - rho) <= rho * (math.expm1(k) + 1e-6), (b, j, u, rho)
+        return "decision"
+    # same n: the drawn token's interval under the oracle weights
+    hid = oracle.spec_oracle._as_f64(inp.hidden)
+    Wf = oracle.spec_oracle._as_f64(inp.W)
+    tp = oracle.lmhead_logits(hid[b * (g + 1) + res.n][None, :], Wf)[0]
+    P = oracle.row_probs(tp, T)
+    if res.n < g:
+        Q = oracle.row_probs(oracle.spec_oracle._as_f64(inp.draft[b, res.n]), T)
+        w = oracle.residual_weights(P, Q)
+        if not np.any(w > 0):
+            w = P
+    else:
+        w = P
+    c = np.cumsum(w)
+    Z = c[-1]
+    t = int(tok[b, n_gpu])
+    lo = (c[t - 1] if t > 0 else 0.0) / Z
+    hi = c[t] / Z
+    u = float(inp.u_resample[b])
+    # each p(x) moves by a factor within exp(+-k); w by at most (e^k - 1) p(x);
+    # both C(t) and Z by at most (e^k - 1), so C/Z by at most 2 (e^k - 1) / Z
+    delta = 2 * math.expm1(k) / Z + 1e-6
+    assert lo - delta <= u < hi + delta, (b, t, res.tokens[n_gpu], lo, hi, u, delta)
+    return "exact" if t == res.tokens[n_gpu] else "token"
+
+
+def test_lmhead_realistic_recipe_full_size_within_envelope(sv, dev):
+    B, gamma, V, H = 64, 4, 262144, 1536
+    W = wl.make_lmhead_W(V, H, seed=0)
+    inp = wl.make_lmhead_round(0, B=B, gamma=gamma, V=V, H=H, W_bits=W)
+    ws = sv.make_workspace(B, gamma, V, H)
+    tok, num, dbg, st = run_lm(sv, to_device_lm(inp, dev), ws)
+    assert st == sv.SPEC_OK
+    seqs = [1, 12, 23, 34, 45, 56]
+    ref = _oracle(inp, seqs)
+    hid = oracle.spec_oracle._as_f64(inp.hidden)
+    Wf = oracle.spec_oracle._as_f64(W)
+    kinds = []
+    for res, b in zip(ref, seqs):
+        eps = _logit_error_bound(hid, Wf, list(range(b * (gamma + 1), (b + 1) * (gamma + 1))))
+        kinds.append(_check_envelope(res, b, inp, tok, num, dbg, eps))
+        # probabilities of the draft tokens: within the envelope too
+        for j in range(gamma):
+            kk = 2 * float(eps.max()) / float(inp.temperature[b])
+            assert abs(dbg[b, j, 0] - res.p_tok[j]) <= res.p_tok[j] * math.expm1(kk) + 1e-5
+            assert abs(dbg[b, j, 1] - res.q_tok[j]) <= 1e-5
+    print("realistic lm_head recipe:", kinds)

@@ -413,6 +413,32 @@ def test_lmhead_logits_bruteforce():
             assert abs(got[r, x] - want) < 1e-15
 
 
+def test_lmhead_verify_groups_rows_per_sequence():
+    """With W the identity (V = H) the lm_head logits are the hidden rows
+    themselves, so the fused verify must reduce to plain sampling verification
+    with target[b, j] = hidden[b*(gamma+1) + j]: pins the row grouping."""
+    rng = np.random.default_rng(31)
+    B, gamma, V = 3, 2, 8
+    hidden = rng.normal(0, 2, (B * (gamma + 1), V))
+    W = np.eye(V)
+    target = hidden.reshape(B, gamma + 1, V)
+    draft = target[:, :gamma] + rng.normal(0, 0.5, (B, gamma, V))
+    toks = rng.integers(0, V, (B, gamma)).astype(np.int32)
+    temp = np.array([1.0, 0.7, 0.0])
+    ua = rng.random((B, gamma))
+    ur = rng.random(B)
+    got = so.verify_lmhead_sample(hidden, W, draft, toks, temp, ua, ur, gamma)
+    want = so.verify_sample(target, draft, toks, temp, ua, ur)
+    for g_, w_ in zip(got, want):
+        assert g_.tokens == w_.tokens and g_.n == w_.n and g_.path == w_.path
+        assert np.allclose(g_.L_p, w_.L_p, rtol=0, atol=1e-12)
+    # a second W (a permutation) permutes the vocabulary of the target rows only
+    perm = rng.permutation(V)
+    got2 = so.verify_lmhead_sample(hidden, W[perm], draft, toks, temp, ua, ur, gamma)
+    want2 = so.verify_sample(target[:, :, perm], draft, toks, temp, ua, ur)
+    assert [r.tokens for r in got2] == [r.tokens for r in want2]
+
+
 # ---------------------------------------------------------------------------
 # speed-up model (host-side closed forms printed on the pages)
 # ---------------------------------------------------------------------------

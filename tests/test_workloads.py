@@ -45,3 +45,28 @@ def test_zipf_profile_and_greedy_drafts():
     assert r.temperature[0] == 0.0 and r.temperature[1] == 1.0
     d = wl.bf16_bits_to_f32(r.draft)
     assert np.array_equal(r.draft_tokens[0], np.argmax(d[0], axis=1))
+
+
+def test_lmhead_exact_sums_recipe_is_exact_in_fp32_any_order():
+    """The exact-sums lm_head recipe: every logit's partial sums are exact in
+    fp32, so a float32 sum in any order equals the float64 dot product."""
+    B, gamma, V, H = 2, 2, 64, 1536
+    W = wl.make_lmhead_W(V, H, seed=0, exact_sums=True)
+    inp = wl.make_lmhead_round(0, B=B, gamma=gamma, V=V, H=H, W_bits=W, exact_sums=True)
+    h = wl.bf16_bits_to_f32(inp.hidden)
+    w = wl.bf16_bits_to_f32(W)
+    assert np.all(np.abs(h) <= 4) and np.all(np.rint(h * 8) == h * 8)
+    assert np.all(np.abs(w) <= 255 / 2048) and np.all(np.rint(w * 2048) == w * 2048)
+    exact = h.astype(np.float64) @ w.astype(np.float64).T
+    rng = np.random.default_rng(5)
+    for r in range(h.shape[0]):
+        for x in range(0, V, 7):
+            prod = (h[r] * w[x]).astype(np.float32)  # exact products
+            for _ in range(3):
+                acc = np.float32(0)
+                for t in prod[rng.permutation(H)]:
+                    acc = np.float32(acc + t)
+                assert float(acc) == exact[r, x]
+    # the realistic recipe is not on the grid
+    inp2 = wl.make_lmhead_round(0, B=B, gamma=gamma, V=V, H=H)
+    assert np.any(np.rint(wl.bf16_bits_to_f32(inp2.hidden) * 8) != wl.bf16_bits_to_f32(inp2.hidden) * 8)

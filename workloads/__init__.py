@@ -15,7 +15,9 @@ describe):
 * longdraft B=128, gamma=8, V=262144,  fp32.  Zipf target; per-sequence sigma ~
             U[0.1, 1.5]; even sequences greedy, odd ones sample at T=1.0.
 * lmhead    hidden [64*5, 1536] ~ N(0,1) bf16; tied embedding W [262144, 1536] ~
-            N(0, 0.02^2) bf16; l_q = bf16(h W^T + N(0, 0.5^2)); T=1.0.
+            N(0, 0.02^2) bf16; l_q = bf16(h W^T + N(0, 0.5^2)); T=1.0.  The
+            exact-sums variant puts h on a 1/8 grid and W on a 2^-11 grid so
+            that h W^T is exact in fp32 in any summation order.
 
 Draft tokens: a sampling sequence draws d_{j+1} from q_j = softmax(l_q[j]/T)
 with the Gumbel-max trick; a greedy sequence (T <= 0) takes argmax l_q[j]
@@ -32,7 +34,7 @@ from dataclasses import dataclass
 import numpy as np
 
 __all__ = ["VerifyInputs", "LmheadInputs", "CONFIGS", "make_round",
-           "make_lmhead_round", "make_custom", "f32_to_bf16_bits",
+           "make_lmhead_round", "make_lmhead_W", "make_custom", "f32_to_bf16_bits",
            "bf16_bits_to_f32", "torch_round", "torch_lmhead_round"]
 
 
@@ -190,23 +192,46 @@ def make_round(config: str, r: int = 0, seed: int = 0, **overrides) -> VerifyInp
                        seed, r, c["rounds"])
 
 
+def make_lmhead_W(V: int = 262144, H: int = 1536, seed: int = 0,
+                  exact_sums: bool = False) -> np.ndarray:
+    """The tied embedding W [V, H] as bf16 bits (seed stream 3).
+
+    exact_sums: W = k / 2048 with k = round(N(0, 0.02^2) * 2048) clipped to
+    [-255, 255] (exact in bf16).  With hidden = k / 8, |k| <= 32, every
+    product h*w is a multiple of 2^-14 and every partial sum of a logit is at
+    most 1536 * 4 * 255/2048 < 2^10 in magnitude, so it is an integer
+    multiple of 2^-14 below 2^24: exact in fp32 whatever the summation order.
+    """
+    c = CONFIGS["lmhead"]
+    wr = _rng(seed, 3)
+    w = wr.normal(0.0, c["w_sd"], size=(V, H)).astype(np.float32)
+    if exact_sums:
+        w = np.clip(np.rint(w * 2048.0), -255, 255).astype(np.float32) / np.float32(2048.0)
+    return f32_to_bf16_bits(w)
+
+
 def make_lmhead_round(r: int = 0, seed: int = 0, B: int = 64, gamma: int = 4,
-                      V: int = 262144, H: int = 1536, W_bits: np.ndarray | None = None
-                      ) -> LmheadInputs:
+                      V: int = 262144, H: int = 1536, W_bits: np.ndarray | None = None,
+                      exact_sums: bool = False, temperature=None) -> LmheadInputs:
     """Round ``r`` of the fused lm_head recipe.  W is fixed across rounds
-    (seed stream 3); pass ``W_bits`` to reuse one already generated."""
+    (seed stream 3); pass ``W_bits`` (from ``make_lmhead_W`` with the same
+    ``exact_sums``) to reuse one already generated.  ``exact_sums`` draws the
+    hidden states on the 1/8 grid (see ``make_lmhead_W``); ``temperature``
+    overrides the recipe's T (a scalar or a per-sequence spec)."""
     c = CONFIGS["lmhead"]
     if W_bits is None:
-        wr = _rng(seed, 3)
-        W_bits = f32_to_bf16_bits(wr.normal(0.0, c["w_sd"], size=(V, H)).astype(np.float32))
+        W_bits = make_lmhead_W(V, H, seed, exact_sums)
     rng = _rng(seed, 4, r)
     R = B * (gamma + 1)
-    hid = f32_to_bf16_bits(rng.normal(0.0, 1.0, size=(R, H)).astype(np.float32))
+    h = rng.normal(0.0, 1.0, size=(R, H)).astype(np.float32)
+    if exact_sums:
+        h = np.clip(np.rint(h * 8.0), -32, 32).astype(np.float32) / np.float32(8.0)
+    hid = f32_to_bf16_bits(h)
     # target logits (fp32) only to derive the draft logits; never an expected value
     tgt = bf16_bits_to_f32(hid) @ bf16_bits_to_f32(W_bits).T
     tgt = tgt.reshape(B, gamma + 1, V)[:, :gamma, :]
     dft = f32_to_bf16_bits(tgt + rng.normal(0.0, c["sigma"], size=tgt.shape).astype(np.float32))
-    temp = np.full(B, c["temperature"], dtype=np.float32)
+    temp = _per_seq(c["temperature"] if temperature is None else temperature, B, rng)
     toks = _draft_tokens(_rng(seed, 5, r), bf16_bits_to_f32(dft), temp)
     ua, ur = _uniforms(seed, c["rounds"], B, gamma, r)
     return LmheadInputs(B, gamma, V, H, hid, W_bits, dft, toks, temp, ua, ur)
