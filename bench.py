@@ -290,8 +290,9 @@ def run_ours(args):
                      "avg_launch_us": round(red_s * 1e6, 3),
                      "timing": f"CUDA events over {nred} back-to-back reduce-only launches on the bench stream"},
         "e2e": e2e,
-        "gpu_launches": 4 * args.steps,
-        "launch": f"CUDA graphs of up to {GRAPH_CHUNK} steps (4 kernels per step), replayed on one stream",
+        "gpu_launches": 2 * args.steps,
+        "launch": f"CUDA graphs of up to {GRAPH_CHUNK} steps (2 kernels per step: row reducer, tail), "
+                  "replayed on one stream",
         "clocks": clocks.summary(n_before),
     }
     if rank == 0 and not args.no_cpu_baseline:
@@ -418,7 +419,92 @@ def other_workloads(sv, dev, stream, args):
                      "B": b, "gamma": g, "V": v, "logits_dtype": c["dtype"], "steps": steps}
         del pool
         torch.cuda.empty_cache()
+    res["lmhead"] = lmhead_workload(sv, dev, stream)
     return res
+
+
+def load_tensor_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), "measured (MEASURED_PEAKS.json bf16_tflops, burst)"
+    return 1900.0, "fallback 1.9 PFLOP/s"
+
+
+def lmhead_workload(sv, dev, stream, steps=200):
+    """Fused lm_head + verify: B=64, gamma=4, V=262144, H=1536 (hidden ~ N(0,1),
+    W ~ N(0, 0.02^2), T=1).  Whole-chain rounds/s, and the lm_head GEMM kernel
+    alone against the tensor and HBM rooflines."""
+    import torch
+
+    import workloads as wl
+    c = wl.CONFIGS["lmhead"]
+    b, g, v, h = c["B"], c["gamma"], c["V"], c["H"]
+    pool = [wl.torch_lmhead_round(0, dev)]
+    pool.append(wl.torch_lmhead_round(1, dev, W=pool[0]["W"]))
+    w = sv.make_workspace(b, g, v, h, device=dev)
+    o = torch.empty((b, g + 1), dtype=torch.int32, device=dev)
+    n = torch.empty((b,), dtype=torch.int32, device=dev)
+
+    def st(i, fn=sv.spec_verify_lmhead_sample):
+        p = pool[i % len(pool)]
+        fn(p["hidden"], p["W"], p["draft"], p["draft_tokens"], p["temperature"], p["u_accept"],
+           p["u_resample"], o, n, w)
+
+    def gemm(i):
+        st(i, sv.spec_verify_lmhead_gemm_only)
+
+    with torch.cuda.stream(stream):
+        st(0)
+    torch.cuda.synchronize()
+    assert sv.spec_verify_status(w, stream) == sv.SPEC_OK
+    loop = GraphLoop(st, steps, stream)
+    loop.run()
+    el = loop.run()
+    del loop
+    assert sv.spec_verify_status(w, stream) == sv.SPEC_OK
+    gl = GraphLoop(gemm, steps, stream)
+    gl.run()
+    gs = gl.run() / steps
+    del gl
+    R = b * (g + 1)
+    flops = 2.0 * R * v * h
+    w_bytes = v * h * 2
+    store_bytes = b * g * v * 4  # fp32 rows j < gamma (all sequences sample at T=1)
+    part_bytes = R * (v // 128) * 16
+    peak_t, tk = load_tensor_peak()
+    peak_b, bk = load_peaks()
+    t_floor = max(flops / (peak_t * 1e12), w_bytes / (peak_b * 1e9))
+    res = {"rounds_per_s": round(steps / el, 1), "us_per_round": round(el / steps * 1e6, 2),
+           "B": b, "gamma": g, "V": v, "H": h, "steps": steps,
+           "gemm_kernel": {"kernel": "lmhead_kernel (tcgen05, 128x128x64 tiles, 3 M-tiles)",
+                           "avg_launch_us": round(gs * 1e6, 2),
+                           "achieved_tflops": round(flops / gs / 1e12, 1), "peak_tflops": peak_t,
+                           "tensor_frac": round(flops / gs / 1e12 / peak_t, 4), "tensor_peak_source": tk,
+                           "algorithmic_bytes": w_bytes + R * h * 2 + store_bytes + part_bytes,
+                           "hbm_gbs": round((w_bytes + R * h * 2 + store_bytes + part_bytes) / gs / 1e9, 1),
+                           "hbm_peak_gbs": peak_b, "hbm_peak_source": bk,
+                           "roofline_floor_us": round(t_floor * 1e6, 2),
+                           "frac_of_roofline": round(t_floor / gs, 4),
+                           "roofline": "max(GEMM FLOPs at the bf16 tensor peak, W bytes at HBM bandwidth)"}}
+    del pool
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_only_lmhead(args):
+    import torch
+
+    import speculative_decoding_verification_54_gb300 as sv
+    from speculative_decoding_verification_54_gb300 import _build
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    _build.build()
+    sv.load()
+    stream = torch.cuda.Stream(device=dev)
+    res = lmhead_workload(sv, dev, stream, steps=max(3, min(args.steps, 1000)))
+    print(json.dumps({"workload": "lmhead", **res}), flush=True)
 
 
 # ---------------------------------------------------------------------------
@@ -476,6 +562,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end host-buffer leg")
     ap.add_argument("--row-loads", choices=("ldg", "tma"), default=None,
                     help="row-reducer load path (default: the library's default, direct loads)")
+    ap.add_argument("--only", choices=("lmhead",), default=None,
+                    help="run one extra workload alone and print its figures (diagnostics, profiling)")
     args = ap.parse_args()
     if args.impl == "reference":
         args.steps = 100 if args.steps is None else args.steps
@@ -486,7 +574,10 @@ def main():
             os.environ["SPECV_ROW_LOADS"] = args.row_loads
         args.steps = 20000 if args.steps is None else args.steps
         args.warmup = 20 if args.warmup is None else max(3, args.warmup)
-        run_ours(args)
+        if args.only == "lmhead":
+            run_only_lmhead(args)
+        else:
+            run_ours(args)
 
 
 if __name__ == "__main__":

@@ -117,7 +117,7 @@ __device__ __forceinline__ float dot_row(const uint4* h4, const uint4* w4, int n
 }
 
 __global__ void __launch_bounds__(kLmTailThreads) lm_tail_kernel(const __grid_constant__ LmTailParams p) {
-  __shared__ float xs[kLmTileN];
+  __shared__ float xs[kLmTileV];
   __shared__ int s_last, s_chunk, s_plain;
   __shared__ F2 s_local;
   const int b = blockIdx.y, part = blockIdx.x;
@@ -144,7 +144,7 @@ __global__ void __launch_bounds__(kLmTailThreads) lm_tail_kernel(const __grid_co
 #pragma unroll
       for (int j = 0; j < kLmMassGroup; ++j) {  // lane l: entries 4l..4l+3 of tile t0+j
         const int t = t0 + j;
-        const size_t e = static_cast<size_t>(t) * kLmTileN + 4 * lane;
+        const size_t e = static_cast<size_t>(t) * kLmTileV + 4 * lane;
         const bool ok = t < c1 && e < static_cast<size_t>(p.V);
         xp4[j] = ok ? __ldcg(reinterpret_cast<const float4*>(lp + e))
                     : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
@@ -201,19 +201,19 @@ __global__ void __launch_bounds__(kLmTailThreads) lm_tail_kernel(const __grid_co
   __syncthreads();
   const int chunk = s_chunk;
   const bool plain = s_plain;
-  const int ncol = min(kLmTileN, p.V - chunk * kLmTileN);
+  const int ncol = min(kLmTileV, p.V - chunk * kLmTileV);
   // the chosen tile's target logits: stored rows j < gamma, recomputed for the bonus row
   const int rowp = residual ? s.n : g;
   if (rowp < g) {
-    const float* lp = p.logits + (static_cast<size_t>(b) * g + rowp) * p.V + static_cast<size_t>(chunk) * kLmTileN;
-    for (int c = threadIdx.x; c < kLmTileN; c += kLmTailThreads) xs[c] = (c < ncol) ? __ldcg(lp + c) : -INFINITY;
+    const float* lp = p.logits + (static_cast<size_t>(b) * g + rowp) * p.V + static_cast<size_t>(chunk) * kLmTileV;
+    for (int c = threadIdx.x; c < kLmTileV; c += kLmTailThreads) xs[c] = (c < ncol) ? __ldcg(lp + c) : -INFINITY;
   } else {
     const uint4* h4 = reinterpret_cast<const uint4*>(p.hidden + static_cast<size_t>(b * (g + 1) + g) * p.H);
-    for (int c = warp; c < kLmTileN; c += kLmTailWarps) {
+    for (int c = warp; c < kLmTileV; c += kLmTailWarps) {
       float x = -INFINITY;
       if (c < ncol) {
         const uint4* w4 =
-            reinterpret_cast<const uint4*>(p.W + (static_cast<size_t>(chunk) * kLmTileN + c) * p.H);
+            reinterpret_cast<const uint4*>(p.W + (static_cast<size_t>(chunk) * kLmTileV + c) * p.H);
         x = dot_row(h4, w4, p.H / 8);
       }
       if (lane == 0) xs[c] = x;
@@ -227,7 +227,7 @@ __global__ void __launch_bounds__(kLmTailThreads) lm_tail_kernel(const __grid_co
   const WeightFn fw = plain ? make_weight(rp, rq, false, s.ks) : f;
   float xq[4] = {0.f, 0.f, 0.f, 0.f};
   if (!plain && 4 * lane < ncol)
-    load_bf16x4(p.draft + (static_cast<size_t>(b) * g + s.n) * p.V + static_cast<size_t>(chunk) * kLmTileN + 4 * lane,
+    load_bf16x4(p.draft + (static_cast<size_t>(b) * g + s.n) * p.V + static_cast<size_t>(chunk) * kLmTileV + 4 * lane,
                 xq);
   float w[4];
   F2 my = f2_from(0.f);
@@ -260,7 +260,7 @@ __global__ void __launch_bounds__(kLmTailThreads) lm_tail_kernel(const __grid_co
     for (int off = 16; off > 0; off >>= 1) last_nz = max(last_nz, __shfl_xor_sync(0xffffffffu, last_nz, off));
     tok = last_nz < 0 ? 0 : last_nz;
   }
-  if (lane == 0) p.dp.out_tokens[b * (g + 1) + s.n] = chunk * kLmTileN + tok;
+  if (lane == 0) p.dp.out_tokens[b * (g + 1) + s.n] = chunk * kLmTileV + tok;
 }
 
 }  // namespace specv

@@ -38,7 +38,8 @@ constexpr int kMaxDevices = 64;
 
 struct DeviceInfo {
   int sms = 0;
-  int path = kLdg;  // row-reducer load path (SPECV_ROW_LOADS=tma selects kTma)
+  int path = kLdg;     // row-reducer load path (SPECV_ROW_LOADS=tma selects kTma)
+  int lm_max_dyn = 0;  // dynamic shared memory the lm_head kernel may use
   bool ready = false;
 };
 DeviceInfo g_dev[kMaxDevices];
@@ -56,9 +57,16 @@ int device_info(DeviceInfo* out) {
     if (cudaFuncSetAttribute(rowstats_kernel<float, kTma>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smem) != cudaSuccess ||
         cudaFuncSetAttribute(rowstats_kernel<__nv_bfloat16, kTma>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
-        cudaFuncSetAttribute(lmhead_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kLmSmemBytes)) != cudaSuccess)
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+      return SPEC_ERR_CUDA;
+    int optin = 0;
+    cudaFuncAttributes fa;
+    if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+        cudaFuncGetAttributes(&fa, lmhead_kernel) != cudaSuccess)
+      return SPEC_ERR_CUDA;
+    d.lm_max_dyn = optin - static_cast<int>(fa.sharedSizeBytes);
+    if (cudaFuncSetAttribute(lmhead_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, d.lm_max_dyn) !=
+        cudaSuccess)
       return SPEC_ERR_CUDA;
     const char* env = std::getenv("SPECV_ROW_LOADS");
     d.path = (env != nullptr && std::strcmp(env, "tma") == 0) ? kTma : kLdg;
@@ -234,7 +242,41 @@ int dispatch(const Common& a, bool sampling) {
 // ---------------------------------------------------------------------------
 // fused lm_head chain
 // ---------------------------------------------------------------------------
-constexpr int kLmMaxRows = kLmMaxMTiles * kLmTileM;  // 384 verify rows per call
+// Shape of the lm_head kernel for R hidden rows: the rows are split into
+// n_chunks chunks of nc (a multiple of 32, at most 256: the MMA's N), the
+// accumulator rotates through n_slots TMEM slots of nc columns, and the two
+// TMA rings take what shared memory allows (deeper W ring first).
+struct LmPlan {
+  int nc, n_chunks, n_slots, w_stages, h_stages;
+  uint32_t h_bytes, smem;
+};
+
+bool lm_plan(int R, int max_dyn, LmPlan* out) {
+  LmPlan p;
+  p.n_chunks = (R + kLmMaxChunk - 1) / kLmMaxChunk;
+  if (p.n_chunks > 2) return false;  // the kernel issues at most two chunks per K step
+  p.nc = (R + 32 * p.n_chunks - 1) / (32 * p.n_chunks) * 32;
+  p.n_slots = static_cast<int>(kLmTmemCols) / p.nc;
+  if (p.n_slots > kLmMaxSlots) p.n_slots = kLmMaxSlots;
+  if (p.n_slots < p.n_chunks) return false;
+  p.h_bytes = static_cast<uint32_t>(p.n_chunks * p.nc) * 128u;
+  // ring depths in order of preference: the hidden ring waits on L2 round
+  // trips every K step, so it keeps its depth before the (prefetched) W ring
+  static const int kDepths[][2] = {{5, 6}, {5, 5}, {5, 4}, {4, 4}, {5, 3}, {4, 3}, {3, 3}, {4, 2}, {3, 2}};
+  bool fit = false;
+  for (const auto& d : kDepths) {
+    if (lm_smem_bytes(d[0], d[1], p.h_bytes, p.nc) <= static_cast<uint32_t>(max_dyn)) {
+      p.w_stages = d[0];
+      p.h_stages = d[1];
+      fit = true;
+      break;
+    }
+  }
+  if (!fit) return false;
+  p.smem = lm_smem_bytes(p.w_stages, p.h_stages, p.h_bytes, p.nc);
+  *out = p;
+  return true;
+}
 
 struct LmLayout {
   Layout base;  // header, draft-row partials, counters
@@ -245,7 +287,7 @@ struct LmLayout {
 LmLayout lm_layout(int B, int gamma, int V) {
   LmLayout L;
   L.base = layout(B, gamma, V);
-  L.n_tiles = (V + kLmTileN - 1) / kLmTileN;
+  L.n_tiles = (V + kLmTileV - 1) / kLmTileV;
   const size_t R = static_cast<size_t>(B) * (gamma + 1);
   size_t off = L.base.total;
   L.tpart = off;
@@ -288,15 +330,15 @@ EncodeTiledFn encoder() {
   return g_encode;
 }
 
-// 2-D bf16 tensor map over a [rows, H] row-major matrix: boxes of 64 x 128
+// 2-D bf16 tensor map over a [rows, H] row-major matrix: boxes of 64 x box_rows
 // (128-byte rows, swizzled as the tcgen05 descriptors expect); rows past the
 // end read as zero.
-bool encode_rows(CUtensorMap* m, const void* base, int rows, int H) {
+bool encode_rows(CUtensorMap* m, const void* base, int rows, int H, int box_rows) {
   EncodeTiledFn enc = encoder();
   if (enc == nullptr) return false;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(rows)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(H) * 2};
-  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kLmTileK), static_cast<cuuint32_t>(kLmTileM)};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kLmTileK), static_cast<cuuint32_t>(box_rows)};
   const cuuint32_t estr[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -350,25 +392,33 @@ int run_lm_chain(const LmArgs& a) {
   }
 
   // 2. target rows: the lm_head GEMM with its statistics epilogue
+  LmPlan plan;
+  if (!lm_plan(R, dev.lm_max_dyn, &plan)) return SPEC_ERR_UNSUPPORTED;
   LmParams lp;
   std::memset(&lp, 0, sizeof(lp));
-  if (!encode_rows(&lp.tmA, a.hidden, R, a.H) || !encode_rows(&lp.tmB, a.W, a.V, a.H)) return SPEC_ERR_CUDA;
+  if (!encode_rows(&lp.tmW, a.W, a.V, a.H, kLmTileV) || !encode_rows(&lp.tmH, a.hidden, R, a.H, plan.nc))
+    return SPEC_ERR_CUDA;
   lp.R = R;
-  lp.n_mtiles = (R + kLmTileM - 1) / kLmTileM;
   lp.V = a.V;
   lp.H = a.H;
   lp.n_tiles = L.n_tiles;
   lp.gamma = a.gamma;
+  lp.nc = plan.nc;
+  lp.n_chunks = plan.n_chunks;
+  lp.n_slots = plan.n_slots;
+  lp.w_stages = plan.w_stages;
+  lp.h_stages = plan.h_stages;
+  lp.h_bytes = plan.h_bytes;
   lp.temperature = a.temperature;
   lp.partials = reinterpret_cast<float4*>(ws + L.tpart);
   lp.logits = reinterpret_cast<float*>(ws + L.logits);
   lp.status = status;
   const int lm_grid = L.n_tiles < dev.sms ? L.n_tiles : dev.sms;
   if (a.gemm_only) {  // first kernel of the call: plain stream order
-    lmhead_kernel<<<lm_grid, kLmThreads, kLmSmemBytes, a.stream>>>(lp);
+    lmhead_kernel<<<lm_grid, kLmThreads, plan.smem, a.stream>>>(lp);
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
   }
-  if (launch_pdl(lmhead_kernel, dim3(lm_grid), dim3(kLmThreads), kLmSmemBytes, a.stream, lp) != cudaSuccess)
+  if (launch_pdl(lmhead_kernel, dim3(lm_grid), dim3(kLmThreads), plan.smem, a.stream, lp) != cudaSuccess)
     return SPEC_ERR_CUDA;
 
   // 3. decision, 4. residual / bonus masses and the draw
