@@ -32,9 +32,12 @@ namespace specv {
 constexpr int kCombineBatch = 8;  // partials each lane loads at once (256 per warp)
 
 // Fold the cpr chunk partials {M, s, argmax, mk} of one row, warp-wide.
-// Loads are issued in batches of 256 so one L2 round trip covers a
-// 262,144-entry bf16 row.  Lane 0's result is the one to use.
+// Loads are issued in batches of 32*kBatch so that a few L2 round trips cover
+// a row (kBatch = 8: one round trip for the 128 partials of a 262,144-entry
+// bf16 row).  Lane 0's result is the one to use.
+template <int kBatch = kCombineBatch>
 __device__ __forceinline__ RowStat combine_row(const float4* P, int cpr, bool sampled) {
+  constexpr int kCombineBatch = kBatch;
   const int lane = threadIdx.x & 31;
   float m = -FLT_MAX, mkmax = kNegHuge;
   int idx = -1;

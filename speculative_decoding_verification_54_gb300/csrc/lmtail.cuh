@@ -14,8 +14,10 @@
 //                     of a sequence draws the token by inverse CDF in
 //                     ascending vocabulary order: the tile from the masses,
 //                     then the entry inside it.  The bonus row gamma is not
-//                     stored, so its chosen tile's 128 logits are recomputed
-//                     as fp32 dot products of the hidden state with W.
+//                     stored: every CTA of a bonus sequence picks the tile
+//                     from the row's tile partials and recomputes its share of
+//                     the tile's 128 logits as fp32 dot products of the hidden
+//                     state with W, for the last CTA to draw from.
 #pragma once
 
 #include <cfloat>
@@ -31,6 +33,13 @@ namespace specv {
 constexpr int kLmTailThreads = 256;
 constexpr int kLmTailWarps = kLmTailThreads / 32;
 constexpr int kLmMassGroup = 8;  // tiles a warp reduces at once (8 x 512 B of fp32 logits)
+constexpr int kLmSmemTiles = 8192;  // tile masses staged in shared memory for the draw (V <= 1,048,576)
+
+// Tile masses staged in shared memory (level 1 scans them with one warp).
+struct SmemMass {
+  const float* m;
+  __device__ __forceinline__ float operator()(int c) const { return m[c]; }
+};
 
 struct LmTailParams {
   const __nv_bfloat16* hidden;  // [R, H], R = B*(gamma+1)
@@ -42,6 +51,7 @@ struct LmTailParams {
   RowStat* rowstat;             // [B*(2*gamma+1)]
   SeqState* seq;                // [B]
   float* mass;                  // [B][n_tiles]
+  float* xsg;                   // [B][128] the bonus row's recomputed tile
   int* tail_done;               // [B*kCounterStride]
   const float* u_resample;
   DecideParams dp;
@@ -74,8 +84,8 @@ __global__ void __launch_bounds__(kLmTailThreads) lm_decide_kernel(const __grid_
   if (gather) in.xp = __ldcg(p.logits + (static_cast<size_t>(b) * g + lane) * p.V + in.d);
   for (int r = warp; r < nrows; r += kLmTailWarps) {
     RowStat st;
-    if (r <= g)
-      st = combine_row(p.tpart + static_cast<size_t>(b * (g + 1) + r) * p.n_tiles, p.n_tiles, !greedy);
+    if (r <= g)  // one partial per 128-entry tile: 2048 for a 262,144-entry row
+      st = combine_row<32>(p.tpart + static_cast<size_t>(b * (g + 1) + r) * p.n_tiles, p.n_tiles, !greedy);
     else
       st = combine_row(p.dpart + static_cast<size_t>(b * slots + r) * p.cpr_d, p.cpr_d, true);
     if (lane == 0) {
@@ -118,9 +128,11 @@ __device__ __forceinline__ float dot_row(const uint4* h4, const uint4* w4, int n
 
 __global__ void __launch_bounds__(kLmTailThreads) lm_tail_kernel(const __grid_constant__ LmTailParams p) {
   __shared__ float xs[kLmTileV];
+  __shared__ float sm_mass[kLmSmemTiles];
   __shared__ int s_last, s_chunk, s_plain;
   __shared__ F2 s_local;
   const int b = blockIdx.y, part = blockIdx.x;
+  const bool staged = p.n_tiles <= kLmSmemTiles;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = p.gamma, slots = 2 * g + 1;
   grid_dep_wait();
@@ -132,10 +144,10 @@ __global__ void __launch_bounds__(kLmTailThreads) lm_tail_kernel(const __grid_co
   const WeightFn f = make_weight(rp, rq, residual, s.ks);
   float* mass = p.mass + static_cast<size_t>(b) * p.n_tiles;
 
-  // ---- this CTA's share of the tile masses ----
-  const int per = (p.n_tiles + gridDim.x - 1) / gridDim.x;
-  const int c0 = min(p.n_tiles, part * per), c1 = min(p.n_tiles, c0 + per);
   if (residual) {
+    // ---- this CTA's share of the tile masses of max(0, p_n - q_n) ----
+    const int per = (p.n_tiles + gridDim.x - 1) / gridDim.x;
+    const int c0 = min(p.n_tiles, part * per), c1 = min(p.n_tiles, c0 + per);
     const float* lp = p.logits + (static_cast<size_t>(b) * g + s.n) * p.V;
     const __nv_bfloat16* lq = p.draft + (static_cast<size_t>(b) * g + s.n) * p.V;
     for (int t0 = c0 + warp * kLmMassGroup; t0 < c1; t0 += kLmTailWarps * kLmMassGroup) {
@@ -160,11 +172,46 @@ __global__ void __launch_bounds__(kLmTailThreads) lm_tail_kernel(const __grid_co
         if (lane == 0 && t0 + j < c1) mass[t0 + j] = m;
       }
     }
-  } else {  // bonus: tile masses of row gamma from its partials, in units of 2^mk
-    const float4* P = p.tpart + static_cast<size_t>(b * (g + 1) + g) * p.n_tiles;
-    for (int c = c0 + threadIdx.x; c < c1; c += kLmTailThreads) {
-      const float4 q = __ldcg(P + c);
-      mass[c] = q.y * ex2(q.w - rp.mk);
+  } else {
+    // ---- bonus: every CTA picks the tile itself from row gamma's tile
+    // partials (level 1), then recomputes its share of that tile's 128
+    // logits as fp32 dot products of the hidden state with W ----
+    const PartialMass pm{p.tpart + static_cast<size_t>(b * (g + 1) + g) * p.n_tiles, rp.mk};
+    if (staged) {
+      for (int c = threadIdx.x; c < p.n_tiles; c += kLmTailThreads) sm_mass[c] = pm(c);
+      __syncthreads();
+    }
+    if (warp == 0) {
+      F2 local;
+      int chunk;
+      if (staged) {
+        const SmemMass sm{sm_mass};
+        const MassScan ms = scan_masses_fn(sm, p.n_tiles);
+        chunk = pick_chunk_fn(sm, ms, f2_mul_f(ms.Z, p.u_resample[b]), &local);
+      } else {
+        const MassScan ms = scan_masses_fn(pm, p.n_tiles);
+        chunk = pick_chunk_fn(pm, ms, f2_mul_f(ms.Z, p.u_resample[b]), &local);
+      }
+      if (lane == 0) {
+        s_chunk = chunk;
+        s_local = local;
+        s_plain = 1;
+      }
+    }
+    __syncthreads();
+    const int chunk = s_chunk;
+    const int ncol = min(kLmTileV, p.V - chunk * kLmTileV);
+    const int per = (kLmTileV + gridDim.x - 1) / gridDim.x;
+    const int lo = min(kLmTileV, part * per), hi = min(kLmTileV, lo + per);
+    const uint4* h4 = reinterpret_cast<const uint4*>(p.hidden + static_cast<size_t>(b * (g + 1) + g) * p.H);
+    for (int c = lo + warp; c < hi; c += kLmTailWarps) {
+      float x = -INFINITY;
+      if (c < ncol) {
+        const uint4* w4 =
+            reinterpret_cast<const uint4*>(p.W + (static_cast<size_t>(chunk) * kLmTileV + c) * p.H);
+        x = dot_row(h4, w4, p.H / 8);
+      }
+      if (lane == 0) p.xsg[b * kLmTileV + c] = x;
     }
   }
   __syncthreads();
@@ -178,13 +225,34 @@ __global__ void __launch_bounds__(kLmTailThreads) lm_tail_kernel(const __grid_co
   if (!s_last) return;
   __threadfence();
 
-  // ---- the draw (last CTA): level 1 picks the tile ----
-  if (warp == 0) {
-    bool plain = !residual;
+  // ---- the draw (last CTA) ----
+  if (residual && staged) {  // level 1 over the residual tile masses, staged in shared memory
+    for (int c = threadIdx.x; c < p.n_tiles; c += kLmTailThreads) sm_mass[c] = __ldcg(mass + c);
+    __syncthreads();
+    if (warp == 0) {
+      const SmemMass sm{sm_mass};
+      MassScan ms = scan_masses_fn(sm, p.n_tiles);
+      const bool z0 = !(ms.Z.hi > 0.f);
+      if (z0) {
+        // Z == 0 cannot happen in exact arithmetic; if rounding produces it,
+        // draw from p_n itself (tile masses from its partials)
+        const PartialMass pn{p.tpart + static_cast<size_t>(b * (g + 1) + s.n) * p.n_tiles, rp.mk};
+        for (int c = lane; c < p.n_tiles; c += 32) sm_mass[c] = pn(c);
+        __syncwarp();
+        ms = scan_masses_fn(sm, p.n_tiles);
+      }
+      F2 local;
+      const int chunk = pick_chunk_fn(sm, ms, f2_mul_f(ms.Z, p.u_resample[b]), &local);
+      if (lane == 0) {
+        s_chunk = chunk;
+        s_local = local;
+        s_plain = z0;
+      }
+    }
+  } else if (residual && warp == 0) {  // level 1 over the residual tile masses in global memory
+    bool plain = false;
     MassScan ms = scan_masses(mass, p.n_tiles);
-    if (residual && !(ms.Z.hi > 0.f)) {
-      // Z == 0 cannot happen in exact arithmetic; if rounding produces it,
-      // draw from p_n itself (tile masses from its partials)
+    if (!(ms.Z.hi > 0.f)) {
       masses_from_partials(p.tpart + static_cast<size_t>(b * (g + 1) + s.n) * p.n_tiles, rp.mk, mass,
                            p.n_tiles);
       ms = scan_masses(mass, p.n_tiles);
@@ -202,22 +270,12 @@ __global__ void __launch_bounds__(kLmTailThreads) lm_tail_kernel(const __grid_co
   const int chunk = s_chunk;
   const bool plain = s_plain;
   const int ncol = min(kLmTileV, p.V - chunk * kLmTileV);
-  // the chosen tile's target logits: stored rows j < gamma, recomputed for the bonus row
-  const int rowp = residual ? s.n : g;
-  if (rowp < g) {
-    const float* lp = p.logits + (static_cast<size_t>(b) * g + rowp) * p.V + static_cast<size_t>(chunk) * kLmTileV;
+  // the chosen tile's target logits: the stored row n, or the bonus row's recomputed tile
+  if (residual) {
+    const float* lp = p.logits + (static_cast<size_t>(b) * g + s.n) * p.V + static_cast<size_t>(chunk) * kLmTileV;
     for (int c = threadIdx.x; c < kLmTileV; c += kLmTailThreads) xs[c] = (c < ncol) ? __ldcg(lp + c) : -INFINITY;
   } else {
-    const uint4* h4 = reinterpret_cast<const uint4*>(p.hidden + static_cast<size_t>(b * (g + 1) + g) * p.H);
-    for (int c = warp; c < kLmTileV; c += kLmTailWarps) {
-      float x = -INFINITY;
-      if (c < ncol) {
-        const uint4* w4 =
-            reinterpret_cast<const uint4*>(p.W + (static_cast<size_t>(chunk) * kLmTileV + c) * p.H);
-        x = dot_row(h4, w4, p.H / 8);
-      }
-      if (lane == 0) xs[c] = x;
-    }
+    for (int c = threadIdx.x; c < kLmTileV; c += kLmTailThreads) xs[c] = __ldcg(p.xsg + b * kLmTileV + c);
   }
   __syncthreads();
   if (warp != 0) return;

@@ -146,13 +146,14 @@ __device__ __forceinline__ float chunk_mass(const SampleParams& p, const WeightF
 }
 
 // Level 1 of the inverse-CDF draw, warp-wide.  Lane l owns the contiguous
-// chunk range [c0, c1) of the chunk masses; the scan gives each lane its own
-// sum and the inclusive sum over lanes, and Z the total.
+// chunk range [c0, c1) of the chunk masses mass(c); the scan gives each lane
+// its own sum and the inclusive sum over lanes, and Z the total.
 struct MassScan {
   F2 lsum, incl, Z;
   int c0, c1;
 };
-__device__ __forceinline__ MassScan scan_masses(const float* mass, int n) {
+template <typename MassFn>
+__device__ __forceinline__ MassScan scan_masses_fn(const MassFn& mass, int n) {
   const int lane = threadIdx.x & 31;
   const int per = (n + 31) / 32;
   MassScan ms;
@@ -160,7 +161,7 @@ __device__ __forceinline__ MassScan scan_masses(const float* mass, int n) {
   ms.c1 = min(n, ms.c0 + per);
   ms.lsum = f2_from(0.f);
 #pragma unroll 4
-  for (int c = ms.c0; c < ms.c1; ++c) ms.lsum = f2_add(ms.lsum, f2_from(__ldcg(mass + c)));
+  for (int c = ms.c0; c < ms.c1; ++c) ms.lsum = f2_add(ms.lsum, f2_from(mass(c)));
   ms.incl = warp_scan_incl(ms.lsum);
   ms.Z = f2_shfl(ms.incl, 31);
   return ms;
@@ -170,7 +171,8 @@ __device__ __forceinline__ MassScan scan_masses(const float* mass, int n) {
 // exceeds it.  *local receives target minus the mass before that chunk, or
 // FLT_MAX when rounding puts the target at or beyond the total, in which case
 // the last chunk of nonzero mass is taken.
-__device__ __forceinline__ int pick_chunk(const float* mass, const MassScan& ms, F2 target, F2* local) {
+template <typename MassFn>
+__device__ __forceinline__ int pick_chunk_fn(const MassFn& mass, const MassScan& ms, F2 target, F2* local) {
   const int lane = threadIdx.x & 31;
   const unsigned over = __ballot_sync(0xffffffffu, f2_gt(ms.incl, target));
   int chunk = -1;
@@ -180,7 +182,7 @@ __device__ __forceinline__ int pick_chunk(const float* mass, const MassScan& ms,
     if (lane == L) {
       F2 run = f2_sub(ms.incl, ms.lsum);
       for (int c = ms.c0; c < ms.c1; ++c) {
-        const F2 nxt = f2_add(run, f2_from(__ldcg(mass + c)));
+        const F2 nxt = f2_add(run, f2_from(mass(c)));
         if (f2_gt(nxt, target)) {
           chunk = c;
           loc = f2_sub(target, run);
@@ -190,7 +192,7 @@ __device__ __forceinline__ int pick_chunk(const float* mass, const MassScan& ms,
       }
       if (chunk < 0) {  // rounding inside the lane: its last nonzero chunk
         for (int c = ms.c1 - 1; c >= ms.c0; --c)
-          if (__ldcg(mass + c) > 0.f) {
+          if (mass(c) > 0.f) {
             chunk = c;
             break;
           }
@@ -202,7 +204,7 @@ __device__ __forceinline__ int pick_chunk(const float* mass, const MassScan& ms,
   if (chunk < 0) {  // u*Z at or beyond the total: the last nonzero chunk
     int last = -1;
     for (int c = ms.c0; c < ms.c1; ++c)
-      if (__ldcg(mass + c) > 0.f) last = c;
+      if (mass(c) > 0.f) last = c;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, off));
     chunk = last < 0 ? 0 : last;
@@ -211,6 +213,30 @@ __device__ __forceinline__ int pick_chunk(const float* mass, const MassScan& ms,
   *local = loc;
   return chunk;
 }
+
+// The same over masses held in global memory (written by other CTAs: read
+// through L2).
+struct GlobalMass {
+  const float* m;
+  __device__ __forceinline__ float operator()(int c) const { return __ldcg(m + c); }
+};
+__device__ __forceinline__ MassScan scan_masses(const float* mass, int n) {
+  return scan_masses_fn(GlobalMass{mass}, n);
+}
+__device__ __forceinline__ int pick_chunk(const float* mass, const MassScan& ms, F2 target, F2* local) {
+  return pick_chunk_fn(GlobalMass{mass}, ms, target, local);
+}
+
+// Chunk masses of a plain row straight from its partials {M, s, argmax, mk},
+// in units of 2^mk (mk: the row's combined scaled max).
+struct PartialMass {
+  const float4* P;
+  float mk;
+  __device__ __forceinline__ float operator()(int c) const {
+    const float4 q = __ldcg(P + c);
+    return q.y * ex2(q.w - mk);
+  }
+};
 
 // Chunk masses of a plain row from its partials {M, s, argmax, mk}, in units
 // of 2^mk (mk: the row's combined scaled max); this lane's range [c0, c1).

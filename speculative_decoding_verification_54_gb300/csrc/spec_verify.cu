@@ -280,7 +280,7 @@ bool lm_plan(int R, int max_dyn, LmPlan* out) {
 
 struct LmLayout {
   Layout base;  // header, draft-row partials, counters
-  size_t tpart, logits, rowstat, seq, mass, total;
+  size_t tpart, logits, rowstat, seq, mass, xsg, total;
   int n_tiles;
 };
 
@@ -300,6 +300,8 @@ LmLayout lm_layout(int B, int gamma, int V) {
   off += align_up(static_cast<size_t>(B) * sizeof(SeqState), 256);
   L.mass = off;
   off += align_up(static_cast<size_t>(B) * L.n_tiles * sizeof(float), 256);
+  L.xsg = off;
+  off += align_up(static_cast<size_t>(B) * kLmTileV * sizeof(float), 256);
   L.total = off;
   return L;
 }
@@ -432,6 +434,7 @@ int run_lm_chain(const LmArgs& a) {
   tp.rowstat = reinterpret_cast<RowStat*>(ws + L.rowstat);
   tp.seq = reinterpret_cast<SeqState*>(ws + L.seq);
   tp.mass = reinterpret_cast<float*>(ws + L.mass);
+  tp.xsg = reinterpret_cast<float*>(ws + L.xsg);
   tp.tail_done = reinterpret_cast<int*>(ws + L.base.tail_done);
   tp.u_resample = a.u_resample;
   tp.B = a.B;
