@@ -35,11 +35,6 @@ constexpr int kLmTailWarps = kLmTailThreads / 32;
 constexpr int kLmMassGroup = 8;  // tiles a warp reduces at once (8 x 512 B of fp32 logits)
 constexpr int kLmSmemTiles = 8192;  // tile masses staged in shared memory for the draw (V <= 1,048,576)
 
-// Tile masses staged in shared memory (level 1 scans them with one warp).
-struct SmemMass {
-  const float* m;
-  __device__ __forceinline__ float operator()(int c) const { return m[c]; }
-};
 
 struct LmTailParams {
   const __nv_bfloat16* hidden;  // [R, H], R = B*(gamma+1)

@@ -21,6 +21,7 @@
 #pragma once
 
 #include <cfloat>
+#include <climits>
 
 #include "common.cuh"
 #include "decide.cuh"
@@ -250,99 +251,130 @@ __device__ __forceinline__ void masses_from_partials(const float4* P, float mk, 
   }
 }
 
-// The inverse-CDF draw for sequence b (warp-wide, one warp of the last CTA).
+constexpr int kTailSmemChunks = 4096;  // chunk masses staged in shared memory for the draw
+
+// Chunk masses staged in shared memory.
+struct SmemMass {
+  const float* m;
+  __device__ __forceinline__ float operator()(int c) const { return m[c]; }
+};
+
+// The inverse-CDF draw for sequence b, by the whole (last) CTA.
 // rs: the sequence's combined rows; s: its decision.
+// Level 1: the CTA stages the chunk masses in shared memory and one warp
+// scans them for the chunk.  Level 2: thread t takes vector t of that chunk
+// (8 bf16 or 4 fp32 entries) and its weights' two-float sum; a block scan of
+// those sums finds the first thread whose prefix passes u*Z minus the mass of
+// the earlier chunks, and that thread walks its own entries.
 template <typename T>
-__device__ __noinline__ void draw_token(const SampleParams& p, int b, const SeqState s,
-                                        const RowStat* rs) {
+__device__ __noinline__ void draw_token(const SampleParams& p, int b, const SeqState s, const RowStat* rs) {
   constexpr int P = Elt<T>::kPerVec;
-  const int lane = threadIdx.x & 31;
+  __shared__ float sm_mass[kTailSmemChunks];
+  __shared__ F2 s_wtot[kTailWarps];
+  __shared__ F2 s_local;
+  __shared__ int s_chunk, s_resid, s_first, s_tok, s_lastnz;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = p.gamma, slots = 2 * g + 1;
   float* mass = p.mass + static_cast<size_t>(b) * p.cpr;
-  bool residual = (s.mode == kModeResidual);
-  const int rowp = residual ? s.n : g;
+  const bool staged = p.cpr <= kTailSmemChunks;
 
   // ---- level 1: which chunk ----
-  MassScan ms = scan_masses(mass, p.cpr);
-  if (residual && !(ms.Z.hi > 0.f)) {
-    // Z == 0 cannot happen in exact arithmetic; if rounding produces it, draw
-    // from p_n itself (chunk masses from the row partials)
-    masses_from_partials(p.partials + static_cast<size_t>(b * slots + s.n) * p.cpr, rs[s.n].mk, mass, p.cpr);
-    ms = scan_masses(mass, p.cpr);
-    residual = false;  // weights of target row n as a plain row
+  if (staged) {
+    for (int c = threadIdx.x; c < p.cpr; c += kTailThreads) sm_mass[c] = __ldcg(mass + c);
+    __syncthreads();
   }
-  F2 local;
-  const int chunk = pick_chunk(mass, ms, f2_mul_f(ms.Z, p.u_resample[b]), &local);
+  if (warp == 0) {
+    bool residual = (s.mode == kModeResidual);
+    F2 local;
+    int chunk;
+    if (staged) {
+      const SmemMass sm{sm_mass};
+      MassScan ms = scan_masses_fn(sm, p.cpr);
+      if (residual && !(ms.Z.hi > 0.f)) {
+        // Z == 0 cannot happen in exact arithmetic; if rounding produces it,
+        // draw from p_n itself (chunk masses from the row partials)
+        const PartialMass pn{p.partials + static_cast<size_t>(b * slots + s.n) * p.cpr, rs[s.n].mk};
+        for (int c = lane; c < p.cpr; c += 32) sm_mass[c] = pn(c);
+        __syncwarp();
+        ms = scan_masses_fn(sm, p.cpr);
+        residual = false;  // weights of target row n as a plain row
+      }
+      chunk = pick_chunk_fn(sm, ms, f2_mul_f(ms.Z, p.u_resample[b]), &local);
+    } else {
+      MassScan ms = scan_masses(mass, p.cpr);
+      if (residual && !(ms.Z.hi > 0.f)) {
+        masses_from_partials(p.partials + static_cast<size_t>(b * slots + s.n) * p.cpr, rs[s.n].mk, mass, p.cpr);
+        ms = scan_masses(mass, p.cpr);
+        residual = false;
+      }
+      chunk = pick_chunk(mass, ms, f2_mul_f(ms.Z, p.u_resample[b]), &local);
+    }
+    if (lane == 0) {
+      s_chunk = chunk;
+      s_local = local;
+      s_resid = residual;
+      s_first = INT_MAX;
+      s_lastnz = -1;
+    }
+  }
+  __syncthreads();
 
-  // ---- level 2: which entry inside the chunk.  The chunk's 256 vectors are
-  // taken in two halves; in each, lane l holds the contiguous vectors
-  // [h*128 + 4l, h*128 + 4l + 4) in registers, so the running sum follows
-  // vocabulary order across lanes. ----
-  constexpr int kHalfVec = 4;
+  // ---- level 2: which entry inside the chunk (block-wide) ----
+  const int chunk = s_chunk;
+  const bool residual = s_resid;
+  const F2 local = s_local;
+  const int rowp = (s.mode == kModeResidual) ? s.n : g;  // the Z = 0 fallback keeps row n
   const WeightFn f = make_weight(rs[rowp], rs[g + 1 + (residual ? s.n : 0)], residual, s.ks);
   const uint4* vp = chunk_vec<T>(p.target, static_cast<size_t>(b) * (g + 1) + rowp, p.V, chunk, p.CE);
-  const uint4* vq = chunk_vec<T>(residual ? p.draft : p.target,
-                                 static_cast<size_t>(b) * (residual ? g : g + 1) + (residual ? s.n : rowp),
-                                 p.V, chunk, p.CE);
-  const int nvec = min(p.CE, p.V - chunk * p.CE) / P;
-  F2 base = f2_from(0.f);
-  int tok = -1, last_all = -1;
-#pragma unroll 1
-  for (int h = 0; h < 2 && tok < 0; ++h) {
-    const int v0 = h * (32 * kHalfVec) + lane * kHalfVec;
-    uint4 a[kHalfVec], q[kHalfVec];
-#pragma unroll
-    for (int j = 0; j < kHalfVec; ++j) {
-      const int i = v0 + j;
-      a[j] = (i < nvec) ? __ldg(vp + i) : neg_inf_vec<T>();
-      q[j] = (i < nvec && residual) ? __ldg(vq + i) : neg_inf_vec<T>();
+  const uint4* vq = residual ? chunk_vec<T>(p.draft, static_cast<size_t>(b) * g + s.n, p.V, chunk, p.CE) : vp;
+  const int nvec = min(p.CE, p.V - chunk * p.CE) / P;  // <= 256 vectors of 16 B
+  const int t = threadIdx.x;
+  float w[P];
+  F2 my = f2_from(0.f);
+  int last_nz = -1;
+  {
+    uint4 a = neg_inf_vec<T>(), q = neg_inf_vec<T>();
+    if (t < nvec) {
+      a = __ldg(vp + t);
+      if (residual) q = __ldg(vq + t);
     }
-    F2 my = f2_from(0.f);
-    int last_nz = -1;
+    float xp[P], xq[P];
+    Elt<T>::unpack(a, xp);
+    Elt<T>::unpack(q, xq);
 #pragma unroll
-    for (int j = 0; j < kHalfVec; ++j) {
-      float xp[P], xq[P];
-      Elt<T>::unpack(a[j], xp);
-      Elt<T>::unpack(q[j], xq);
-      float t = 0.f;
-#pragma unroll
-      for (int k = 0; k < P; ++k) {
-        const float w = f(xp[k], xq[k]);
-        t += w;
-        if (w > 0.f) last_nz = (v0 + j) * P + k;
-      }
-      my = f2_add(my, f2_from(t));
+    for (int k = 0; k < P; ++k) {
+      w[k] = (t < nvec) ? f(xp[k], xq[k]) : 0.f;
+      my = f2_add(my, f2_from(w[k]));
+      if (w[k] > 0.f) last_nz = t * P + k;
     }
-    const F2 cincl = f2_add(warp_scan_incl(my), base);
-    const unsigned cover = __ballot_sync(0xffffffffu, f2_gt(cincl, local));
-    if (cover) {
-      const int L = __ffs(cover) - 1;
-      if (lane == L) {
-        F2 run = f2_sub(cincl, my);
-#pragma unroll
-        for (int j = 0; j < kHalfVec; ++j) {
-          float xp[P], xq[P];
-          Elt<T>::unpack(a[j], xp);
-          Elt<T>::unpack(q[j], xq);
-#pragma unroll
-          for (int k = 0; k < P; ++k) {
-            run = f2_add(run, f2_from(f(xp[k], xq[k])));
-            if (tok < 0 && f2_gt(run, local)) tok = (v0 + j) * P + k;
-          }
-        }
-        if (tok < 0) tok = last_nz;  // rounding inside the lane
-      }
-      tok = __shfl_sync(0xffffffffu, tok, L);
-    }
-    base = f2_shfl(cincl, 31);
-    last_all = max(last_all, last_nz);
   }
-  if (tok < 0) {  // beyond the chunk total: its last nonzero entry
+  F2 incl = warp_scan_incl(my);
+  if (lane == 31) s_wtot[warp] = incl;
+  __syncthreads();
+  F2 wpre = f2_from(0.f);
+  for (int w2 = 0; w2 < warp; ++w2) wpre = f2_add(wpre, s_wtot[w2]);
+  incl = f2_add(incl, wpre);
+  // the prefix sums are non-decreasing in t: the first thread whose inclusive
+  // prefix passes `local` holds the entry
+  if (f2_gt(incl, local)) atomicMin(&s_first, t);
+  if (last_nz >= 0) atomicMax(&s_lastnz, last_nz);
+  __syncthreads();
+  if (t == s_first) {
+    F2 run = f2_sub(incl, my);
+    int tok = -1;
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) last_all = max(last_all, __shfl_xor_sync(0xffffffffu, last_all, off));
-    tok = last_all < 0 ? 0 : last_all;
+    for (int k = 0; k < P; ++k) {
+      run = f2_add(run, f2_from(w[k]));
+      if (tok < 0 && f2_gt(run, local)) tok = t * P + k;
+    }
+    s_tok = (tok >= 0) ? tok : last_nz;  // rounding inside the thread: its last nonzero entry
   }
-  if (lane == 0) p.dp.out_tokens[b * (g + 1) + s.n] = chunk * p.CE + tok;
+  __syncthreads();
+  if (t == 0) {
+    // beyond the chunk total (rounding): the chunk's last nonzero entry
+    const int tok = (s_first != INT_MAX && s_tok >= 0) ? s_tok : (s_lastnz < 0 ? 0 : s_lastnz);
+    p.dp.out_tokens[b * (g + 1) + s.n] = chunk * p.CE + tok;
+  }
 }
 
 template <typename T>
@@ -399,7 +431,7 @@ __global__ void __launch_bounds__(kTailThreads, 1) tail_kernel(const __grid_cons
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  if (warp == 0) draw_token<T>(p, b, s, rs);
+  draw_token<T>(p, b, s, rs);
 }
 
 }  // namespace specv

@@ -222,9 +222,10 @@ int run_chain(const Common& a, bool sampling) {
   dp.status = status;
   dp.gamma = a.gamma;
   dp.V = a.V;
-  // parts per sequence: about two CTAs per SM over the batch (at most 16);
-  // greedy calls need one (no residual pass)
-  int parts = sampling ? (2 * dev.sms + a.B - 1) / a.B : 1;
+  // parts per sequence: about one CTA per SM over the batch (at most 16), so
+  // the tail's CTAs start as soon as the row reducer frees the SMs; greedy
+  // calls need one (no residual pass)
+  int parts = sampling ? (dev.sms + a.B - 1) / a.B : 1;
   if (parts > 16) parts = 16;
   if (parts > pl.cpr) parts = pl.cpr;
   if (parts < 1) parts = 1;
