@@ -419,7 +419,50 @@ def other_workloads(sv, dev, stream, args):
                      "B": b, "gamma": g, "V": v, "logits_dtype": c["dtype"], "steps": steps}
         del pool
         torch.cuda.empty_cache()
+    res["multi"] = multi_workload(sv, dev, stream)
     res["lmhead"] = lmhead_workload(sv, dev, stream)
+    return res
+
+
+def multi_workload(sv, dev, stream, steps=1000):
+    """Several draft candidates per sequence: B=8 sequences x 4 candidates,
+    gamma=4, V=262144, bf16, greedy (candidates of a sequence share row 0).
+    Rounds/s and the logit GB/s the call streams."""
+    import torch
+
+    import workloads as wl
+    B, n, g, v = 8, 4, 4, 262144
+    pool = []
+    for r in range(3):  # 3 x 83.9 MB > L2
+        p = wl.torch_round("batched", r, dev, B=B * n, temperature=0.0)
+        t = p["target"].view(B, n, g + 1, v).clone()
+        t[:, 1:, 0, :] = t[:, :1, 0, :]
+        pool.append(dict(target=t.contiguous(), draft_tokens=p["draft_tokens"].view(B, n, g).contiguous()))
+        del p
+    w = sv.make_workspace(B * n, g, v, device=dev)
+    o = torch.empty((B, g + 1), dtype=torch.int32, device=dev)
+    nn = torch.empty((B,), dtype=torch.int32, device=dev)
+    ch = torch.empty((B,), dtype=torch.int32, device=dev)
+
+    def st(i):
+        p = pool[i % len(pool)]
+        sv.spec_verify_greedy_multi(p["target"], p["draft_tokens"], o, nn, w, out_choice=ch)
+
+    with torch.cuda.stream(stream):
+        st(0)
+    torch.cuda.synchronize()
+    loop = GraphLoop(st, steps, stream)
+    loop.run()
+    el = loop.run()
+    del loop
+    assert sv.spec_verify_status(w, stream) == sv.SPEC_OK
+    nb = B * n * (g + 1) * v * 2
+    rps = steps / el
+    res = {"rounds_per_s": round(rps, 1), "us_per_round": round(el / steps * 1e6, 2),
+           "logit_gbs": round(rps * nb / 1e9, 1), "frac_of_8tbs": round(rps * nb / 1e9 / NOMINAL_HBM_GBS, 4),
+           "B": B, "n_cand": n, "gamma": g, "V": v, "logits_dtype": "bf16", "mode": "greedy", "steps": steps}
+    del pool
+    torch.cuda.empty_cache()
     return res
 
 

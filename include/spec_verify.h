@@ -92,6 +92,31 @@ int spec_verify_greedy(const void *target_logits, spec_dtype dt,
                        void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Greedy verification of several draft candidates per sequence ("Accelerating
+ * Gemma 4: faster inference with multi-token prediction drafters", §6 进阶优化
+ * 与扩展思路, item 2 多候选草稿): the target verifies n candidate drafts in one
+ * pass and the candidate with the longest accepted prefix is kept.
+ *
+ *   target_logits [B, n_cand, gamma+1, V] (dtype dt)  rows of candidate c of
+ *                                                     sequence b: its path's
+ *                                                     verify positions
+ *   draft_tokens  [B, n_cand, gamma] int32
+ *   out_tokens [B, gamma+1], out_num_accepted [B]     as spec_verify_greedy,
+ *                                                     for the kept candidate
+ *   out_choice    optional [B] int32 (NULL to skip)   the kept candidate's index
+ *
+ * Each candidate is verified as in spec_verify_greedy; the kept one has the
+ * most accepted drafts, the lowest candidate index on ties.  The workspace
+ * must come from spec_verify_workspace_bytes(B * n_cand, gamma, V, 0);
+ * B * n_cand must not exceed 65535.
+ */
+int spec_verify_greedy_multi(const void *target_logits, spec_dtype dt,
+                             const int32_t *draft_tokens, int B, int n_cand, int gamma,
+                             int V, int32_t *out_tokens, int32_t *out_num_accepted,
+                             int32_t *out_choice, void *workspace, size_t workspace_bytes,
+                             void *stream);
+
+/*
  * Rejection-sampling verification ("Gemma 4 Multi-Token Prediction (MTP)
  * 深度解析", §2.2 推测解码的数学保证; "第 8 章 …", section 为什么输出不会变;
  * "自投机解码 …", §3.2 采样解码 and §3.3 随机数与 batch 内对齐).

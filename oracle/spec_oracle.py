@@ -59,6 +59,7 @@ __all__ = [
     "verify_sample",
     "lmhead_logits",
     "verify_lmhead_sample",
+    "verify_greedy_multi",
 ]
 
 
@@ -274,6 +275,29 @@ def verify_sample(target, draft, draft_tokens, temperature, u_accept,
     return [verify_sample_seq(target[b], draft[b], draft_tokens[b],
                               temperature[b], u_accept[b], u_resample[b])
             for b in idx]
+
+
+# ---------------------------------------------------------------------------
+# several draft candidates per sequence ([MTP-blog] §6 进阶优化与扩展思路, item
+# 2 多候选草稿: the target verifies n candidate drafts at once and the one with
+# the longest accepted length is kept)
+# ---------------------------------------------------------------------------
+def verify_greedy_multi(target, draft_tokens) -> list[tuple[SeqResult, int]]:
+    """target [B, n, gamma+1, V]: the target's rows for each candidate path;
+    draft_tokens [B, n, gamma].  Each candidate is verified greedily on its
+    own rows; the kept candidate is the one with the most accepted drafts, the
+    lowest candidate index on ties.  Returns (its SeqResult, its index) per
+    sequence."""
+    out = []
+    for b in range(len(draft_tokens)):
+        res = [verify_greedy_seq(target[b][c], draft_tokens[b][c])
+               for c in range(len(draft_tokens[b]))]
+        best = 0
+        for c in range(1, len(res)):
+            if res[c].n > res[best].n:
+                best = c
+        out.append((res[best], best))
+    return out
 
 
 # ---------------------------------------------------------------------------

@@ -24,6 +24,7 @@ from .binding import (  # noqa: F401
     load,
     make_workspace,
     spec_verify_greedy,
+    spec_verify_greedy_multi,
     spec_verify_lmhead_gemm_only,
     spec_verify_lmhead_sample,
     spec_verify_sample,

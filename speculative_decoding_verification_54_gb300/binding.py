@@ -29,6 +29,7 @@ EXPORTED = (
     "spec_verify_sample", "spec_verify_status", "spec_verify_error_string",
     "spec_verify_version", "spec_verify_selftest_timeout", "spec_verify_sample_reduce_only",
     "spec_verify_sample_noalloc", "spec_verify_lmhead_sample", "spec_verify_lmhead_gemm_only",
+    "spec_verify_greedy_multi",
 )
 
 
@@ -58,6 +59,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.spec_verify_workspace_bytes.argtypes = [_i, _i, _i, _i, ctypes.POINTER(_sz)]
     lib.spec_verify_workspace_init.argtypes = [_vp, _sz, _vp]
     lib.spec_verify_greedy.argtypes = [_vp, _i, _vp, _i, _i, _i, _vp, _vp, _vp, _sz, _vp]
+    lib.spec_verify_greedy_multi.argtypes = [_vp, _i, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _sz, _vp]
     lib.spec_verify_sample.argtypes = [_vp, _vp, _i, _vp, _vp, _vp, _vp, _i, _i, _i,
                                        _vp, _vp, _vp, _vp, _sz, _vp]
     lib.spec_verify_sample_reduce_only.argtypes = list(lib.spec_verify_sample.argtypes)
@@ -155,6 +157,18 @@ def spec_verify_greedy(target_logits, draft_tokens, out_tokens, out_num_accepted
                                      _ptr(draft_tokens), B, gamma, V, _ptr(out_tokens),
                                      _ptr(out_num_accepted), _ptr(workspace), _nbytes(workspace),
                                      _stream(stream)), "spec_verify_greedy")
+
+
+def spec_verify_greedy_multi(target_logits, draft_tokens, out_tokens, out_num_accepted, workspace,
+                             out_choice=None, stream=None) -> None:
+    """target_logits [B, n_cand, gamma+1, V] (fp32/bf16), draft_tokens
+    [B, n_cand, gamma] int32; out_tokens [B, gamma+1], out_num_accepted [B],
+    optional out_choice [B] int32.  Workspace: make_workspace(B * n_cand, gamma, V)."""
+    B, n_cand, g1, V = target_logits.shape
+    _check(load().spec_verify_greedy_multi(_ptr(target_logits), _dtype_code(target_logits),
+                                           _ptr(draft_tokens), B, n_cand, g1 - 1, V, _ptr(out_tokens),
+                                           _ptr(out_num_accepted), _ptr(out_choice), _ptr(workspace),
+                                           _nbytes(workspace), _stream(stream)), "spec_verify_greedy_multi")
 
 
 def spec_verify_sample(target_logits, draft_logits, draft_tokens, temperature, u_accept,

@@ -208,4 +208,39 @@ __device__ __forceinline__ void decide_sequence(const DecideParams& p, int b, co
   }
 }
 
+// Several draft candidates per sequence ("Accelerating Gemma 4: faster
+// inference with multi-token prediction drafters" §6, item 2 多候选草稿): each
+// candidate was verified greedily as a sequence of its own (rows b*n + c);
+// keep the one with the most accepted drafts, the lowest candidate index on
+// ties.  One warp per sequence.
+__global__ void __launch_bounds__(32) select_candidate_kernel(const int32_t* cand_tokens, const int32_t* cand_num,
+                                                               int n_cand, int gamma, int32_t* out_tokens,
+                                                               int32_t* out_num, int32_t* out_choice) {
+  grid_dep_wait();
+  const int b = blockIdx.x, lane = threadIdx.x;
+  int best_n = -1, best_c = n_cand;
+  for (int c = lane; c < n_cand; c += 32) {  // c grows within a lane: strict > keeps the lowest
+    const int nn = cand_num[b * n_cand + c];
+    if (nn > best_n) {
+      best_n = nn;
+      best_c = c;
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const int on = __shfl_xor_sync(0xffffffffu, best_n, off);
+    const int oc = __shfl_xor_sync(0xffffffffu, best_c, off);
+    if (on > best_n || (on == best_n && oc < best_c)) {
+      best_n = on;
+      best_c = oc;
+    }
+  }
+  const int32_t* src = cand_tokens + static_cast<size_t>(b * n_cand + best_c) * (gamma + 1);
+  for (int j = lane; j <= gamma; j += 32) out_tokens[b * (gamma + 1) + j] = src[j];
+  if (lane == 0) {
+    out_num[b] = best_n;
+    if (out_choice != nullptr) out_choice[b] = best_c;
+  }
+}
+
 }  // namespace specv

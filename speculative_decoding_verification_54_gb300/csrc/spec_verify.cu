@@ -77,7 +77,7 @@ int device_info(DeviceInfo* out) {
 }
 
 struct Layout {
-  size_t header, partials, mass, tail_done, total;
+  size_t header, partials, mass, tail_done, cand, total;
 };
 
 // Offsets of the workspace regions for a call with (B, gamma, V); sized for
@@ -95,6 +95,8 @@ Layout layout(int B, int gamma, int V) {
   off += align_up(static_cast<size_t>(B) * cpr * sizeof(float), 256);
   L.tail_done = off;  // per-sequence counters: zero when no call is running
   off += align_up(static_cast<size_t>(B) * kCounterStride * sizeof(int), 256);
+  L.cand = off;  // per-candidate outputs of the multi-candidate entry: tokens [B, gamma+1], counts [B]
+  off += align_up(static_cast<size_t>(B) * (gamma + 2) * sizeof(int32_t), 256);
   L.total = off;
   return L;
 }
@@ -135,8 +137,8 @@ Plan make_plan(int B, int gamma, int V, size_t esize, int sms, bool sampling, in
   return make_plan_rows(B * (sampling ? (2 * gamma + 1) : (gamma + 1)), V, esize, sms, path);
 }
 
-template <typename Kern, typename Params>
-cudaError_t launch_pdl(Kern k, dim3 grid, dim3 block, size_t smem, cudaStream_t s, const Params& prm) {
+template <typename Kern, typename... Args>
+cudaError_t launch_pdl(Kern k, dim3 grid, dim3 block, size_t smem, cudaStream_t s, const Args&... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
@@ -147,7 +149,7 @@ cudaError_t launch_pdl(Kern k, dim3 grid, dim3 block, size_t smem, cudaStream_t 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k, prm);
+  return cudaLaunchKernelEx(&cfg, k, args...);
 }
 
 struct Common {
@@ -531,6 +533,47 @@ int spec_verify_greedy(const void* target_logits, spec_dtype dt, const int32_t* 
   a.ws_bytes = workspace_bytes;
   a.stream = static_cast<cudaStream_t>(stream);
   return dispatch(a, false);
+}
+
+int spec_verify_greedy_multi(const void* target_logits, spec_dtype dt, const int32_t* draft_tokens, int B,
+                             int n_cand, int gamma, int V, int32_t* out_tokens, int32_t* out_num_accepted,
+                             int32_t* out_choice, void* workspace, size_t workspace_bytes, void* stream) {
+  if (target_logits == nullptr || draft_tokens == nullptr || out_tokens == nullptr ||
+      out_num_accepted == nullptr)
+    return SPEC_ERR_INVALID_ARG;
+  if (n_cand < 1 || B < 1 || static_cast<long long>(B) * n_cand > 65535) return SPEC_ERR_INVALID_ARG;
+  const int BN = B * n_cand;
+  if (int e = check_shape(BN, gamma, V)) return e;
+  if (dt != SPEC_F32 && dt != SPEC_BF16) return SPEC_ERR_UNSUPPORTED;
+  if (!aligned16(target_logits)) return SPEC_ERR_ALIGNMENT;
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return SPEC_ERR_WORKSPACE;
+  const Layout L = layout(BN, gamma, V);
+  if (workspace_bytes < L.total) return SPEC_ERR_WORKSPACE;
+  // every candidate is verified greedily as a sequence of its own (rows
+  // b*n_cand + c), into the workspace; then one warp per sequence keeps the
+  // best candidate
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int32_t* cand_tokens = reinterpret_cast<int32_t*>(ws + L.cand);
+  int32_t* cand_num = cand_tokens + static_cast<size_t>(BN) * (gamma + 1);
+  Common a = {};
+  a.target = target_logits;
+  a.dt = dt;
+  a.draft_tokens = draft_tokens;
+  a.B = BN;
+  a.gamma = gamma;
+  a.V = V;
+  a.out_tokens = cand_tokens;
+  a.out_num = cand_num;
+  a.ws = workspace;
+  a.ws_bytes = workspace_bytes;
+  a.stream = static_cast<cudaStream_t>(stream);
+  if (int e = dispatch(a, false)) return e;
+  if (launch_pdl(select_candidate_kernel, dim3(B), dim3(32), 0, a.stream, cand_tokens,
+                 static_cast<const int32_t*>(cand_num), n_cand, gamma, out_tokens, out_num_accepted,
+                 out_choice) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+  return SPEC_OK;
 }
 
 static int sample_entry(bool reduce_only, const void* target_logits, const void* draft_logits, spec_dtype dt,

@@ -174,3 +174,30 @@ def test_lmhead_workspace_bytes(lib):
         with pytest.raises(sv.SpecVerifyError) as e:
             sv.spec_verify_workspace_bytes(*bad)
         assert e.value.code == code
+
+
+def _multi(lib, **kw):
+    args = dict(t=A16, dt=sv.SPEC_BF16, tok=A16, B=4, n=3, g=4, V=4096, out=A16, num=A16, ch=None, ws=WS,
+                wsb=1 << 30)
+    args.update(kw)
+    return lib.spec_verify_greedy_multi(args["t"], args["dt"], args["tok"], args["B"], args["n"], args["g"],
+                                        args["V"], args["out"], args["num"], args["ch"], args["ws"], args["wsb"],
+                                        None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(t=None), sv.SPEC_ERR_INVALID_ARG),
+    (dict(tok=None), sv.SPEC_ERR_INVALID_ARG),
+    (dict(out=None), sv.SPEC_ERR_INVALID_ARG),
+    (dict(n=0), sv.SPEC_ERR_INVALID_ARG),
+    (dict(B=0), sv.SPEC_ERR_INVALID_ARG),
+    (dict(B=20000, n=4), sv.SPEC_ERR_INVALID_ARG),   # B * n_cand > 65535
+    (dict(g=32), sv.SPEC_ERR_INVALID_ARG),
+    (dict(V=12), sv.SPEC_ERR_INVALID_ARG),
+    (dict(dt=5), sv.SPEC_ERR_UNSUPPORTED),
+    (dict(t=A8), sv.SPEC_ERR_ALIGNMENT),
+    (dict(ws=None), sv.SPEC_ERR_WORKSPACE),
+    (dict(wsb=4096), sv.SPEC_ERR_WORKSPACE),
+])
+def test_greedy_multi_rejects_bad_arguments_on_host(lib, kw, code):
+    assert _multi(lib, **kw) == code

@@ -165,6 +165,68 @@ def test_greedy_speculation_equals_plain_argmax_chain():
 
 
 # ---------------------------------------------------------------------------
+# several draft candidates ("Accelerating Gemma 4…" §6, item 2 多候选草稿)
+# ---------------------------------------------------------------------------
+def _cand_drafts(lm, pre, gamma, c):
+    """Greedy drafts of candidate c: its own noisy draft model (salt per c)."""
+    cur, drafts = list(pre), []
+    for _ in range(gamma):
+        lq = lm.target_logits(cur) + lm.dn * _toy_logits(tuple(cur), lm.salt + 1000 + 17 * c, lm.V, 1.0)
+        d = int(np.argmax(lq))
+        drafts.append(d)
+        cur.append(d)
+    return drafts
+
+
+def multi_candidate_failures(verify_multi=None):
+    """Decode with n candidates per round; the output must be the plain argmax
+    chain, and each round must keep as many drafts as the best candidate's
+    common prefix with that chain."""
+    verify_multi = verify_multi or so.verify_greedy_multi
+    bad = 0
+    for salt in range(4):
+        for gamma in (2, 4):
+            for n_cand in (2, 3, 5):
+                lm = ToyLM(V=8, salt=salt, draft_noise=1.2)
+                chain = _greedy_chain(lm, [salt % 8], 40)
+                pre, out = [salt % 8], []
+                while len(out) < 24:
+                    cands = [_cand_drafts(lm, pre, gamma, c) for c in range(n_cand)]
+                    target = np.stack([np.stack([lm.target_logits(pre + d[:j]) for j in range(gamma + 1)])
+                                       for d in cands])[None]
+                    res, choice = verify_multi(target, np.array(cands)[None])[0]
+                    ref = chain[len(out):len(out) + gamma + 1]
+                    best = max(next((j for j in range(gamma) if d[j] != ref[j]), gamma) for d in cands)
+                    emitted = res.tokens[:res.n + 1]
+                    bad += (res.n != best) + (emitted != ref[:len(emitted)]) + (cands[choice][:res.n] != ref[:res.n])
+                    out += emitted
+                    pre += emitted
+    return bad
+
+
+def test_multi_candidate_keeps_the_longest_and_matches_the_argmax_chain():
+    assert multi_candidate_failures() == 0
+
+
+def test_multi_candidate_ties_and_single_candidate():
+    rng = np.random.default_rng(41)
+    g, V = 3, 16
+    rows = rng.normal(0, 2, (g + 1, V))
+    chain = [int(np.argmax(rows[j])) for j in range(g)]
+    bad_draft = [(chain[0] + 1) % V] + chain[1:]
+    # two equally good candidates: the lower index is kept
+    t = np.stack([rows, rows])[None]
+    res, choice = so.verify_greedy_multi(t, np.array([[chain, chain]]))[0]
+    assert choice == 0 and res.n == g
+    # the strictly better candidate wins wherever it sits
+    res, choice = so.verify_greedy_multi(t, np.array([[bad_draft, chain]]))[0]
+    assert choice == 1 and res.n == g
+    # one candidate: plain greedy verification
+    res, choice = so.verify_greedy_multi(rows[None, None], np.array([[bad_draft]]))[0]
+    assert choice == 0 and res.tokens == so.verify_greedy_seq(rows, bad_draft).tokens
+
+
+# ---------------------------------------------------------------------------
 # exhaustive enumeration: the output marginal equals the target's own
 # autoregressive distribution ("Gemma 4 MTP 深度解析" §2.2; "第 8 章…" 为什么输出不会变)
 # ---------------------------------------------------------------------------
@@ -517,3 +579,26 @@ def test_mutation_icdf_off_by_one_is_caught(monkeypatch):
         return min(k + 1, len(w) - 1), m
     monkeypatch.setattr(so, "inverse_cdf", shifted)
     assert first_token_chi2(mod=so, rounds=5000) > 29.0
+
+
+def test_mutation_multi_candidate_rules_are_caught(monkeypatch):
+    """Keeping the shortest candidate, or the last of equal ones, fails a pin."""
+    def shortest(target, draft_tokens):
+        out = []
+        for b in range(len(draft_tokens)):
+            res = [so.verify_greedy_seq(target[b][c], draft_tokens[b][c]) for c in range(len(draft_tokens[b]))]
+            best = min(range(len(res)), key=lambda c: res[c].n)
+            out.append((res[best], best))
+        return out
+    assert multi_candidate_failures(shortest) > 0
+
+    def last_of_equal(target, draft_tokens):
+        out = []
+        for b in range(len(draft_tokens)):
+            res = [so.verify_greedy_seq(target[b][c], draft_tokens[b][c]) for c in range(len(draft_tokens[b]))]
+            best = max(range(len(res)), key=lambda c: (res[c].n, c))
+            out.append((res[best], best))
+        return out
+    monkeypatch.setattr(so, "verify_greedy_multi", last_of_equal)
+    with pytest.raises(AssertionError):
+        test_multi_candidate_ties_and_single_candidate()

@@ -34,7 +34,7 @@ from dataclasses import dataclass
 import numpy as np
 
 __all__ = ["VerifyInputs", "LmheadInputs", "CONFIGS", "make_round",
-           "make_lmhead_round", "make_lmhead_W", "make_custom", "f32_to_bf16_bits",
+           "make_lmhead_round", "make_lmhead_W", "make_custom", "make_multi", "f32_to_bf16_bits",
            "bf16_bits_to_f32", "torch_round", "torch_lmhead_round"]
 
 
@@ -179,6 +179,21 @@ def make_custom(B: int, gamma: int, V: int, dtype: str = "f32", profile: str = "
     ua, ur = _uniforms(seed, rounds, B, gamma, r)
     return VerifyInputs(B, gamma, V, dtype, np.ascontiguousarray(tgt_s),
                         np.ascontiguousarray(dft_s), toks, temp, ua, ur)
+
+
+def make_multi(B: int, n_cand: int, gamma: int = 4, V: int = 4096, dtype: str = "f32",
+               profile: str = "normal", seed: int = 0, r: int = 0):
+    """Several draft candidates per sequence: B*n_cand candidate paths drawn
+    with ``make_custom`` (greedy drafts from draft logits with a per-path
+    noise scale in [0.2, 1.5]), grouped [B, n_cand, ...].  Every candidate of
+    a sequence starts from the same prefix, so their row 0 is made identical.
+    Returns (target [B, n, gamma+1, V], draft_tokens [B, n, gamma])."""
+    inp = make_custom(B * n_cand, gamma, V, dtype, profile, 2.0, ("uniform", 0.2, 1.5), 0.0,
+                      seed, r, 1)
+    tgt = inp.target.reshape(B, n_cand, gamma + 1, V).copy()
+    tgt[:, 1:, 0, :] = tgt[:, :1, 0, :]
+    toks = inp.draft_tokens.reshape(B, n_cand, gamma).copy()
+    return tgt, toks
 
 
 def make_round(config: str, r: int = 0, seed: int = 0, **overrides) -> VerifyInputs:
