@@ -51,7 +51,8 @@ enum {
   SPEC_ERR_WORKSPACE = -4,    /* workspace null, misaligned or too small        */
   SPEC_ERR_CUDA = -5,         /* a CUDA runtime call or kernel launch failed    */
   SPEC_ERR_TIMEOUT = -6,      /* device side: a bounded wait ran out            */
-  SPEC_ERR_DEVICE_INPUT = -7  /* device side: a draft token outside [0, V)      */
+  SPEC_ERR_DEVICE_INPUT = -7, /* device side: a draft token outside [0, V)      */
+  SPEC_ERR_STATE = -8         /* host round driver: inconsistent bookkeeping   */
 };
 
 #define SPEC_MAX_GAMMA 31
@@ -230,6 +231,42 @@ int spec_verify_lmhead_gemm_only(const void *hidden, const void *W, const void *
                                  int gamma, int V, int H, int32_t *out_tokens,
                                  int32_t *out_num_accepted, float *out_debug,
                                  void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Host bookkeeping after a verify round (HOST pointers; no GPU work).
+ *
+ * Per sequence the caller keeps seq_len (prompt + emitted tokens), kv_len
+ * (entries in the target's KV cache) and gamma (the next round's draft
+ * length).  Between rounds the newest token has no KV entry yet, so
+ * kv_len == seq_len - 1.  Given num_accepted[b] = n from the verify call
+ * (0 <= n <= gamma), spec_round_update sets, for every sequence:
+ *   seq_len += n + 1   (accepted drafts + the replacement / resampled / bonus
+ *                       token: "第 8 章 …", 多出来的那一个 token 从哪来)
+ *   kv_len  += n + 1   and kv_keep[b] = the new kv_len: the verify pass
+ *                       appended gamma + 1 entries; the caller keeps the first
+ *                       kv_keep[b] and drops the rest ("自投机解码 …" §3.3:
+ *                       trim to the accepted length; cache and sequence
+ *                       lengths must agree after every round)
+ *   gamma   += 2 if n == gamma, else gamma -= 1, clamped to
+ *                       [gamma_min, gamma_max] ("Gemma 4 Multi-Token
+ *                       Prediction (MTP) 深度解析" §5.1, the heuristic
+ *                       schedule; the page finds drafts beyond about 10
+ *                       tokens rarely pay)
+ * All sequences are checked first (kv_len == seq_len - 1, 0 <= n <= gamma,
+ * gamma >= 1): if one fails, nothing is changed, *first_bad (optional) gets
+ * its index and SPEC_ERR_STATE is returned.  Bad arguments (NULL states or
+ * counts, B < 0, gamma_min < 1, gamma_max > SPEC_MAX_GAMMA, gamma_min >
+ * gamma_max) return SPEC_ERR_INVALID_ARG.  kv_keep [B] may be NULL.
+ */
+typedef struct {
+  int32_t gamma;
+  int32_t reserved;
+  int64_t seq_len;
+  int64_t kv_len;
+} spec_round_state;
+
+int spec_round_update(spec_round_state *states, const int32_t *num_accepted, int B,
+                      int gamma_min, int gamma_max, int64_t *kv_keep, int *first_bad);
 
 /*
  * Synchronise `stream`, then return the device-side status recorded in

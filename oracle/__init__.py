@@ -7,5 +7,7 @@ from .spec_oracle import *  # noqa: F401,F403
 from .spec_oracle import __all__ as _core_all
 from .analysis import *  # noqa: F401,F403
 from .analysis import __all__ as _analysis_all
+from .rounds import *  # noqa: F401,F403
+from .rounds import __all__ as _rounds_all
 
-__all__ = list(_core_all) + list(_analysis_all)
+__all__ = list(_core_all) + list(_analysis_all) + list(_rounds_all)

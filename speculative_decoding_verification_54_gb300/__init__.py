@@ -15,14 +15,17 @@ from .binding import (  # noqa: F401
     SPEC_ERR_INVALID_ARG,
     SPEC_ERR_TIMEOUT,
     SPEC_ERR_UNSUPPORTED,
+    SPEC_ERR_STATE,
     SPEC_ERR_WORKSPACE,
     SPEC_F32,
     SPEC_OK,
+    SpecRoundState,
     SpecVerifyError,
     error_string,
     lib_path,
     load,
     make_workspace,
+    spec_round_update,
     spec_verify_greedy,
     spec_verify_greedy_multi,
     spec_verify_lmhead_gemm_only,

@@ -11,7 +11,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libspecverify.so")
-SOURCES = ["spec_verify.cu"]
+SOURCES = ["spec_verify.cu", "round_driver.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -23,7 +23,7 @@ def nvcc_path() -> str:
 
 
 def _inputs():
-    files = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cu", ".cuh"))]
+    files = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cu", ".cuh", ".cpp"))]
     files.append(os.path.join(INCLUDE, "spec_verify.h"))
     files.append(os.path.abspath(__file__))
     return files

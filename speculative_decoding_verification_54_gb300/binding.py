@@ -22,6 +22,7 @@ SPEC_ERR_WORKSPACE = -4
 SPEC_ERR_CUDA = -5
 SPEC_ERR_TIMEOUT = -6
 SPEC_ERR_DEVICE_INPUT = -7
+SPEC_ERR_STATE = -8
 MAX_GAMMA = 31
 
 EXPORTED = (
@@ -29,7 +30,7 @@ EXPORTED = (
     "spec_verify_sample", "spec_verify_status", "spec_verify_error_string",
     "spec_verify_version", "spec_verify_selftest_timeout", "spec_verify_sample_reduce_only",
     "spec_verify_sample_noalloc", "spec_verify_lmhead_sample", "spec_verify_lmhead_gemm_only",
-    "spec_verify_greedy_multi",
+    "spec_verify_greedy_multi", "spec_round_update",
 )
 
 
@@ -68,6 +69,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.spec_verify_lmhead_sample.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i,
                                               _vp, _vp, _vp, _vp, _sz, _vp]
     lib.spec_verify_lmhead_gemm_only.argtypes = list(lib.spec_verify_lmhead_sample.argtypes)
+    lib.spec_round_update.argtypes = [_vp, _vp, _i, _i, _i, _vp, _vp]
     lib.spec_verify_status.argtypes = [_vp, _vp]
     lib.spec_verify_error_string.argtypes = [_i]
     lib.spec_verify_error_string.restype = ctypes.c_char_p
@@ -253,6 +255,28 @@ def spec_verify_lmhead_gemm_only(hidden, W, draft_logits, draft_tokens, temperat
     _lmhead_call(load().spec_verify_lmhead_gemm_only, "spec_verify_lmhead_gemm_only", hidden, W,
                  draft_logits, draft_tokens, temperature, u_accept, u_resample, out_tokens,
                  out_num_accepted, workspace, out_debug, stream)
+
+
+class SpecRoundState(ctypes.Structure):
+    """spec_round_state: per-sequence host bookkeeping of the round driver."""
+    _fields_ = [("gamma", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("seq_len", ctypes.c_int64), ("kv_len", ctypes.c_int64)]
+
+
+def spec_round_update(states, num_accepted, gamma_min: int, gamma_max: int):
+    """Host round bookkeeping.  ``states``: a ctypes array of SpecRoundState
+    (updated in place); ``num_accepted``: host int sequence.  Returns the
+    number of KV entries to keep per sequence.  Raises SpecVerifyError
+    (SPEC_ERR_STATE, with the first inconsistent sequence) on bad bookkeeping."""
+    B = len(states)
+    n = (ctypes.c_int32 * B)(*[int(x) for x in num_accepted])
+    keep = (ctypes.c_int64 * B)()
+    bad = ctypes.c_int(-1)
+    code = load().spec_round_update(ctypes.cast(states, _vp) if B else None, ctypes.cast(n, _vp),
+                                    B, gamma_min, gamma_max, ctypes.cast(keep, _vp), ctypes.byref(bad))
+    _check(code, f"spec_round_update (first bad sequence {bad.value})" if code == SPEC_ERR_STATE
+           else "spec_round_update")
+    return list(keep)
 
 
 def spec_verify_status(workspace, stream=None) -> int:

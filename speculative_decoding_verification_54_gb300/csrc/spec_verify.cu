@@ -486,6 +486,7 @@ const char* spec_verify_error_string(int code) {
     case SPEC_ERR_CUDA: return "CUDA runtime error";
     case SPEC_ERR_TIMEOUT: return "device wait timed out";
     case SPEC_ERR_DEVICE_INPUT: return "draft token outside [0, V)";
+    case SPEC_ERR_STATE: return "inconsistent round bookkeeping (kv_len != seq_len - 1 or accepted > gamma)";
     default: return "unknown error";
   }
 }

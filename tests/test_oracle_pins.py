@@ -602,3 +602,48 @@ def test_mutation_multi_candidate_rules_are_caught(monkeypatch):
     monkeypatch.setattr(so, "verify_greedy_multi", last_of_equal)
     with pytest.raises(AssertionError):
         test_multi_candidate_ties_and_single_candidate()
+
+
+# ---------------------------------------------------------------------------
+# host round bookkeeping ("自投机解码…" §3.3; "Gemma 4 MTP 深度解析" §5.1)
+# ---------------------------------------------------------------------------
+def test_round_update_against_an_explicit_kv_cache():
+    """Simulate the cache as a list of token ids: the verify pass appends the
+    newest token and the gamma drafts, the rejected tail is dropped.  After
+    every round the cache must hold exactly the sequence minus its newest
+    token, and the oracle's kept length must equal the simulated one."""
+    rng = np.random.default_rng(13)
+    for trial in range(50):
+        seq = list(rng.integers(0, 100, int(rng.integers(1, 20))))
+        cache = seq[:-1]
+        st = oracle.RoundState(gamma=int(rng.integers(1, 9)), seq_len=len(seq), kv_len=len(cache))
+        for _ in range(30):
+            g = st.gamma
+            drafts = list(rng.integers(0, 100, g))
+            n = int(rng.integers(0, g + 1))
+            cache = cache + [seq[-1]] + drafts          # the verify pass
+            emitted = drafts[:n] + [int(rng.integers(0, 100))]
+            cache = cache[:len(seq) + n]                # drop entries of rejected drafts
+            seq = seq + emitted
+            keep = oracle.round_update(st, n, 1, 10)
+            assert keep == len(cache) == st.kv_len and st.seq_len == len(seq)
+            assert cache == seq[:-1]
+
+
+def test_round_update_gamma_schedule_and_errors():
+    st = oracle.RoundState(gamma=4, seq_len=7, kv_len=6)
+    oracle.round_update(st, 4, 1, 10)   # every draft accepted: +2
+    assert st.gamma == 6
+    oracle.round_update(st, 2, 1, 10)   # a rejection: -1
+    assert st.gamma == 5
+    for _ in range(5):
+        oracle.round_update(st, st.gamma, 1, 10)
+    assert st.gamma == 10               # capped
+    for _ in range(20):
+        oracle.round_update(st, 0, 1, 10)
+    assert st.gamma == 1                # floored
+    with pytest.raises(ValueError):
+        oracle.round_update(st, 2, 1, 10)          # more accepted than drafted
+    bad = oracle.RoundState(gamma=4, seq_len=7, kv_len=7)
+    with pytest.raises(ValueError):
+        oracle.round_update(bad, 1, 1, 10)         # cache and sequence disagree
