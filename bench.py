@@ -419,8 +419,44 @@ def other_workloads(sv, dev, stream, args):
                      "B": b, "gamma": g, "V": v, "logits_dtype": c["dtype"], "steps": steps}
         del pool
         torch.cuda.empty_cache()
+    res["topkp"] = topkp_workload(sv, dev, stream)
     res["multi"] = multi_workload(sv, dev, stream)
     res["lmhead"] = lmhead_workload(sv, dev, stream)
+    return res
+
+
+def topkp_workload(sv, dev, stream, steps=1000, top_k=64, top_p=0.95):
+    """The batched workload with top-k / top-p truncation of p and q
+    (top_k=64, top_p=0.95): rounds/s and the logit GB/s the call streams."""
+    import torch
+
+    import workloads as wl
+    B, g, v = 32, 4, 262144
+    pool = [wl.torch_round("batched", r, dev) for r in range(POOL)]
+    w = sv.make_topkp_workspace(B, g, v, device=dev)
+    o = torch.empty((B, g + 1), dtype=torch.int32, device=dev)
+    nn = torch.empty((B,), dtype=torch.int32, device=dev)
+
+    def st(i):
+        p = pool[i % len(pool)]
+        sv.spec_verify_sample_topkp(p["target"], p["draft"], p["draft_tokens"], p["temperature"],
+                                    p["u_accept"], p["u_resample"], top_k, top_p, o, nn, w)
+
+    with torch.cuda.stream(stream):
+        st(0)
+    torch.cuda.synchronize()
+    loop = GraphLoop(st, steps, stream)
+    loop.run()
+    el = loop.run()
+    del loop
+    assert sv.spec_verify_status(w, stream) == sv.SPEC_OK
+    nb = sum(counted_bytes(B, g, v, 2, int((p["temperature"] > 0).sum().item())) for p in pool) / len(pool)
+    rps = steps / el
+    res = {"rounds_per_s": round(rps, 1), "us_per_round": round(el / steps * 1e6, 2),
+           "logit_gbs": round(rps * nb / 1e9, 1), "frac_of_8tbs": round(rps * nb / 1e9 / NOMINAL_HBM_GBS, 4),
+           "B": B, "gamma": g, "V": v, "logits_dtype": "bf16", "top_k": top_k, "top_p": top_p, "steps": steps}
+    del pool
+    torch.cuda.empty_cache()
     return res
 
 
@@ -536,6 +572,20 @@ def lmhead_workload(sv, dev, stream, steps=200):
     return res
 
 
+def run_only_topkp(args):
+    import torch
+
+    import speculative_decoding_verification_54_gb300 as sv
+    from speculative_decoding_verification_54_gb300 import _build
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    _build.build()
+    sv.load()
+    stream = torch.cuda.Stream(device=dev)
+    res = topkp_workload(sv, dev, stream, steps=max(3, min(args.steps, 2000)))
+    print(json.dumps({"workload": "topkp", **res}), flush=True)
+
+
 def run_only_lmhead(args):
     import torch
 
@@ -605,7 +655,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end host-buffer leg")
     ap.add_argument("--row-loads", choices=("ldg", "tma"), default=None,
                     help="row-reducer load path (default: the library's default, direct loads)")
-    ap.add_argument("--only", choices=("lmhead",), default=None,
+    ap.add_argument("--only", choices=("lmhead", "topkp"), default=None,
                     help="run one extra workload alone and print its figures (diagnostics, profiling)")
     args = ap.parse_args()
     if args.impl == "reference":
@@ -619,6 +669,8 @@ def main():
         args.warmup = 20 if args.warmup is None else max(3, args.warmup)
         if args.only == "lmhead":
             run_only_lmhead(args)
+        elif args.only == "topkp":
+            run_only_topkp(args)
         else:
             run_ours(args)
 

@@ -147,6 +147,40 @@ int spec_verify_sample(const void *target_logits, const void *draft_logits,
                        size_t workspace_bytes, void *stream);
 
 /*
+ * Rejection-sampling verification with top-k / top-p truncation applied
+ * identically to the target and the draft distributions ("Gemma 4
+ * Multi-Token Prediction (MTP) 深度解析" §5.1 samples with top_k=64,
+ * top_p=0.95 next to the drafter; "第 8 章 …", 为什么输出不会变: whatever
+ * transforms the target distribution must transform the draft the same way).
+ *
+ * Per row, at the sequence's temperature T:
+ *   K  = tokens with fewer than top_k strictly larger logits (ties at the
+ *        top_k-th value stay in);
+ *   K' = tokens of K whose strictly more likely tokens hold less than top_p of
+ *        softmax(l/T) over K (tie groups stay together);
+ *   p' = softmax(l/T) over K', 0 elsewhere; q' likewise.
+ * Then the rule of spec_verify_sample with p', q': accept iff
+ * u_accept < p'(d)/q'(d) (q'(d) = 0: accepted); draw position n from
+ * max(0, p'_n - q'_n) or the bonus from p'_gamma by inverse CDF in ascending
+ * vocabulary order.  out_debug's normalisers are those of the truncated rows.
+ *
+ * Same arguments as spec_verify_sample plus 1 <= top_k <= 1024 and
+ * 0 < top_p <= 1 (else SPEC_ERR_INVALID_ARG).  A row whose K holds more than
+ * 2048 entries (massive ties) makes spec_verify_status return
+ * SPEC_ERR_UNSUPPORTED.  The workspace comes from
+ * spec_verify_topkp_workspace_bytes.
+ */
+int spec_verify_topkp_workspace_bytes(int B, int gamma, int V, size_t *bytes);
+
+int spec_verify_sample_topkp(const void *target_logits, const void *draft_logits,
+                             spec_dtype dt, const int32_t *draft_tokens,
+                             const float *temperature, const float *u_accept,
+                             const float *u_resample, int B, int gamma, int V,
+                             int top_k, float top_p, int32_t *out_tokens,
+                             int32_t *out_num_accepted, float *out_debug,
+                             void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Timing / profiling aid: the same arguments and checks as
  * spec_verify_sample, but only the first kernel of its launch chain (the
  * vocab-row reducer, which streams every logit the call reads) is enqueued,

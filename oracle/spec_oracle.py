@@ -60,6 +60,9 @@ __all__ = [
     "lmhead_logits",
     "verify_lmhead_sample",
     "verify_greedy_multi",
+    "truncate_probs",
+    "verify_sample_topkp_seq",
+    "verify_sample_topkp",
 ]
 
 
@@ -161,6 +164,8 @@ class SeqResult:
     p_tok, q_tok: p_j(d_{j+1}) and q_j(d_{j+1}) for j < gamma (nan if greedy).
     L_p, L_q: ln-normalisers of target rows 0..gamma and draft rows 0..gamma-1.
     path: "greedy", "residual", "bonus" or "residual_z0".
+    trunc_margin: with top-k / top-p truncation, the smallest distance (in
+        probability mass) between a top-p cut and top_p (inf otherwise).
     """
 
     tokens: list
@@ -171,6 +176,7 @@ class SeqResult:
     L_p: list = field(default_factory=list)
     L_q: list = field(default_factory=list)
     path: str = "greedy"
+    trunc_margin: float = math.inf
 
 
 def verify_greedy_seq(target_rows, draft_tokens) -> SeqResult:
@@ -196,34 +202,12 @@ def verify_greedy_seq(target_rows, draft_tokens) -> SeqResult:
     return SeqResult(tokens=tokens, n=n, path="greedy")
 
 
-def verify_sample_seq(target_rows, draft_rows, draft_tokens, temperature,
-                      u_accept, u_resample) -> SeqResult:
-    """Rejection-sampling verification of one sequence.
-
-    p_j = softmax(l_p[j] / T), q_j = softmax(l_q[j] / T).  Walking j = 0, 1, ...
-    the draft d_{j+1} is accepted iff u_accept[j] < p_j(d)/q_j(d), i.e. with
-    probability min(1, p/q) ([MTP-deep] §2.2; [Book-ch8] 为什么输出不会变;
-    [Self-spec] §3.2).  The first rejection n stops the walk and the later
-    drafts are discarded ([Self-spec] §2.1, §3.3).  Position n is then drawn
-    from max(0, p_n - q_n) / Z by inverse CDF with u_resample; if all gamma
-    drafts pass, it is drawn from p_gamma instead (the bonus token,
-    [Book-ch8] 多出来的那一个 token 从哪来).  Each sequence brings its own uniforms
-    ([Self-spec] §3.3).
-    """
-    T = float(temperature)
-    if T <= 0.0:
-        return verify_greedy_seq(target_rows, draft_tokens)
-    tp = _as_f64(target_rows)
-    tq = _as_f64(draft_rows)
-    d = [int(x) for x in draft_tokens]
+def _decide_and_draw(P, Q, d, u_accept, u_resample, L_p, L_q) -> SeqResult:
+    """The sampling decision on probability rows P[0..gamma], Q[0..gamma-1]:
+    accept d_{j+1} iff u_accept[j] < P[j][d]/Q[j][d], stop at the first
+    rejection n, then draw position n by inverse CDF from max(0, P[n] - Q[n])
+    (from P[gamma] if every draft passed)."""
     gamma = len(d)
-    assert tp.shape[0] == gamma + 1 and tq.shape[0] == gamma
-
-    L_p = [row_log_normaliser(tp[j], T) for j in range(gamma + 1)]
-    L_q = [row_log_normaliser(tq[j], T) for j in range(gamma)]
-    P = [np.exp(tp[j] / T - L_p[j]) for j in range(gamma + 1)]
-    Q = [np.exp(tq[j] / T - L_q[j]) for j in range(gamma)]
-
     p_tok, q_tok = [], []
     margin = math.inf
     n = gamma
@@ -256,6 +240,112 @@ def verify_sample_seq(target_rows, draft_rows, draft_tokens, temperature,
                      q_tok=q_tok, L_p=L_p, L_q=L_q, path=path)
 
 
+def verify_sample_seq(target_rows, draft_rows, draft_tokens, temperature,
+                      u_accept, u_resample) -> SeqResult:
+    """Rejection-sampling verification of one sequence.
+
+    p_j = softmax(l_p[j] / T), q_j = softmax(l_q[j] / T).  Walking j = 0, 1, ...
+    the draft d_{j+1} is accepted iff u_accept[j] < p_j(d)/q_j(d), i.e. with
+    probability min(1, p/q) ([MTP-deep] §2.2; [Book-ch8] 为什么输出不会变;
+    [Self-spec] §3.2).  The first rejection n stops the walk and the later
+    drafts are discarded ([Self-spec] §2.1, §3.3).  Position n is then drawn
+    from max(0, p_n - q_n) / Z by inverse CDF with u_resample; if all gamma
+    drafts pass, it is drawn from p_gamma instead (the bonus token,
+    [Book-ch8] 多出来的那一个 token 从哪来).  Each sequence brings its own uniforms
+    ([Self-spec] §3.3).
+    """
+    T = float(temperature)
+    if T <= 0.0:
+        return verify_greedy_seq(target_rows, draft_tokens)
+    tp = _as_f64(target_rows)
+    tq = _as_f64(draft_rows)
+    d = [int(x) for x in draft_tokens]
+    gamma = len(d)
+    assert tp.shape[0] == gamma + 1 and tq.shape[0] == gamma
+
+    L_p = [row_log_normaliser(tp[j], T) for j in range(gamma + 1)]
+    L_q = [row_log_normaliser(tq[j], T) for j in range(gamma)]
+    P = [np.exp(tp[j] / T - L_p[j]) for j in range(gamma + 1)]
+    Q = [np.exp(tq[j] / T - L_q[j]) for j in range(gamma)]
+    return _decide_and_draw(P, Q, d, u_accept, u_resample, L_p, L_q)
+
+
+# ---------------------------------------------------------------------------
+# top-k / top-p truncation, applied identically to target and draft
+# ([MTP-deep] §5.1: sampling with top_k=64, top_p=0.95 next to the drafter;
+# [Book-ch8] 为什么输出不会变: whatever transforms the target distribution must
+# transform the draft distribution the same way)
+# ---------------------------------------------------------------------------
+def truncate_probs(logits, temperature: float, top_k: int, top_p: float):
+    """The truncated distribution of one row: returns (p, margin).
+
+    K  = tokens with fewer than top_k strictly larger logits (ties at the k-th
+         value stay in);
+    pk = softmax(l / T) over K;
+    K' = tokens x of K whose strictly more likely tokens in K hold less than
+         top_p of pk (a tie group stays together; the most likely tokens are
+         always kept);
+    p  = softmax(l / T) over K', 0 elsewhere.
+    margin = min over x in K of |mass strictly above x - top_p|: how far the
+    top-p cut is from flipping (inf when top_p >= 1).
+    """
+    l = _as_f64(logits)
+    z = l / float(temperature)
+    order = np.argsort(-l, kind="stable")          # descending; ties by index
+    ls = l[order]
+    # top-k with ties: keep x iff #{y : l_y > l_x} < k
+    greater = np.searchsorted(-ls, -ls, side="left")   # count of strictly larger values
+    in_k = greater < top_k
+    idx_k = order[in_k]
+    zk = z[idx_k]
+    pk = np.exp(zk - (zk.max() + np.log(np.sum(np.exp(zk - zk.max())))))
+    lk = l[idx_k]
+    # mass strictly above each kept token (sorted descending, ties grouped)
+    cum = np.concatenate([[0.0], np.cumsum(pk)])
+    first = np.searchsorted(-lk, -lk, side="left")
+    above = cum[first]
+    keep = above < top_p
+    margin = math.inf if top_p >= 1.0 else float(np.min(np.abs(above - top_p)))
+    kept = idx_k[keep]
+    p = np.zeros_like(l)
+    zz = z[kept]
+    m = zz.max()
+    p[kept] = np.exp(zz - m - np.log(np.sum(np.exp(zz - m))))
+    return p, margin
+
+
+def verify_sample_topkp_seq(target_rows, draft_rows, draft_tokens, temperature,
+                            top_k, top_p, u_accept, u_resample) -> SeqResult:
+    """Rejection-sampling verification with both p_j and q_j truncated by
+    ``truncate_probs`` (same T, top_k, top_p).  L_p, L_q are the ln
+    normalisers of the truncated rows (ln of the sum of exp(l/T) over the
+    kept tokens); ``trunc_margin`` is the smallest top-p cut margin of the
+    rows used."""
+    T = float(temperature)
+    if T <= 0.0:
+        return verify_greedy_seq(target_rows, draft_tokens)
+    tp = _as_f64(target_rows)
+    tq = _as_f64(draft_rows)
+    d = [int(x) for x in draft_tokens]
+    gamma = len(d)
+    P, Q, L_p, L_q, tm = [], [], [], [], math.inf
+    for j in range(gamma + 1):
+        pj, mj = truncate_probs(tp[j], T, top_k, top_p)
+        P.append(pj)
+        kept = pj > 0
+        L_p.append(row_log_normaliser(np.where(kept, tp[j], -np.inf), T))
+        tm = min(tm, mj)
+    for j in range(gamma):
+        qj, mj = truncate_probs(tq[j], T, top_k, top_p)
+        Q.append(qj)
+        kept = qj > 0
+        L_q.append(row_log_normaliser(np.where(kept, tq[j], -np.inf), T))
+        tm = min(tm, mj)
+    res = _decide_and_draw(P, Q, d, u_accept, u_resample, L_p, L_q)
+    res.trunc_margin = tm
+    return res
+
+
 # ---------------------------------------------------------------------------
 # batches: sequences are independent ([Self-spec] §3.3: per-sequence counts)
 # ---------------------------------------------------------------------------
@@ -274,6 +364,15 @@ def verify_sample(target, draft, draft_tokens, temperature, u_accept,
     idx = range(len(draft_tokens)) if seqs is None else seqs
     return [verify_sample_seq(target[b], draft[b], draft_tokens[b],
                               temperature[b], u_accept[b], u_resample[b])
+            for b in idx]
+
+
+def verify_sample_topkp(target, draft, draft_tokens, temperature, top_k, top_p,
+                        u_accept, u_resample, seqs=None) -> list[SeqResult]:
+    """Batch form of ``verify_sample_topkp_seq`` (same layout as verify_sample)."""
+    idx = range(len(draft_tokens)) if seqs is None else seqs
+    return [verify_sample_topkp_seq(target[b], draft[b], draft_tokens[b], temperature[b],
+                                    top_k, top_p, u_accept[b], u_resample[b])
             for b in idx]
 
 

@@ -24,6 +24,7 @@ from .binding import (  # noqa: F401
     error_string,
     lib_path,
     load,
+    make_topkp_workspace,
     make_workspace,
     spec_round_update,
     spec_verify_greedy,
@@ -32,10 +33,12 @@ from .binding import (  # noqa: F401
     spec_verify_lmhead_sample,
     spec_verify_sample,
     spec_verify_sample_noalloc,
+    spec_verify_sample_topkp,
     spec_verify_sample_reduce_only,
     spec_verify_selftest_timeout,
     spec_verify_status,
     spec_verify_version,
+    spec_verify_topkp_workspace_bytes,
     spec_verify_workspace_bytes,
     spec_verify_workspace_init,
 )

@@ -30,7 +30,8 @@ EXPORTED = (
     "spec_verify_sample", "spec_verify_status", "spec_verify_error_string",
     "spec_verify_version", "spec_verify_selftest_timeout", "spec_verify_sample_reduce_only",
     "spec_verify_sample_noalloc", "spec_verify_lmhead_sample", "spec_verify_lmhead_gemm_only",
-    "spec_verify_greedy_multi", "spec_round_update",
+    "spec_verify_greedy_multi", "spec_round_update", "spec_verify_topkp_workspace_bytes",
+    "spec_verify_sample_topkp",
 )
 
 
@@ -70,6 +71,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
                                               _vp, _vp, _vp, _vp, _sz, _vp]
     lib.spec_verify_lmhead_gemm_only.argtypes = list(lib.spec_verify_lmhead_sample.argtypes)
     lib.spec_round_update.argtypes = [_vp, _vp, _i, _i, _i, _vp, _vp]
+    lib.spec_verify_topkp_workspace_bytes.argtypes = [_i, _i, _i, ctypes.POINTER(_sz)]
+    lib.spec_verify_sample_topkp.argtypes = [_vp, _vp, _i, _vp, _vp, _vp, _vp, _i, _i, _i, _i, ctypes.c_float,
+                                             _vp, _vp, _vp, _vp, _sz, _vp]
     lib.spec_verify_status.argtypes = [_vp, _vp]
     lib.spec_verify_error_string.argtypes = [_i]
     lib.spec_verify_error_string.restype = ctypes.c_char_p
@@ -190,6 +194,37 @@ def spec_verify_sample(target_logits, draft_logits, draft_tokens, temperature, u
                                      _ptr(out_tokens), _ptr(out_num_accepted), _ptr(out_debug),
                                      _ptr(workspace), _nbytes(workspace), _stream(stream)),
            "spec_verify_sample")
+
+
+def spec_verify_topkp_workspace_bytes(B: int, gamma: int, V: int) -> int:
+    out = _sz(0)
+    _check(load().spec_verify_topkp_workspace_bytes(B, gamma, V, ctypes.byref(out)),
+           "spec_verify_topkp_workspace_bytes")
+    return out.value
+
+
+def make_topkp_workspace(B: int, gamma: int, V: int, device="cuda"):
+    """Allocate (torch) and zero a workspace for spec_verify_sample_topkp."""
+    import torch
+    n = spec_verify_topkp_workspace_bytes(B, gamma, V)
+    ws = torch.zeros(n + 256, dtype=torch.uint8, device=device)
+    off = (-ws.data_ptr()) % 256
+    return ws[off:off + n]
+
+
+def spec_verify_sample_topkp(target_logits, draft_logits, draft_tokens, temperature, u_accept,
+                             u_resample, top_k, top_p, out_tokens, out_num_accepted, workspace,
+                             out_debug=None, stream=None) -> None:
+    """spec_verify_sample with top-k / top-p truncation of p and q (same
+    arguments plus top_k, top_p).  Workspace: make_topkp_workspace(B, gamma, V)."""
+    B, g1, V = target_logits.shape
+    if draft_logits.dtype != target_logits.dtype:
+        raise SpecVerifyError(SPEC_ERR_UNSUPPORTED, "target and draft logits differ in dtype")
+    _check(load().spec_verify_sample_topkp(
+        _ptr(target_logits), _ptr(draft_logits), _dtype_code(target_logits), _ptr(draft_tokens),
+        _ptr(temperature), _ptr(u_accept), _ptr(u_resample), B, g1 - 1, V, int(top_k), float(top_p),
+        _ptr(out_tokens), _ptr(out_num_accepted), _ptr(out_debug), _ptr(workspace), _nbytes(workspace),
+        _stream(stream)), "spec_verify_sample_topkp")
 
 
 def spec_verify_sample_reduce_only(target_logits, draft_logits, draft_tokens, temperature,

@@ -28,6 +28,7 @@
 #include "sample.cuh"
 #include "spec_verify.h"
 #include "tc.cuh"
+#include "topkp.cuh"
 
 using namespace specv;
 
@@ -240,6 +241,72 @@ int dispatch(const Common& a, bool sampling) {
   if (a.dt == SPEC_F32) return run_chain<float>(a, sampling);
   if (a.dt == SPEC_BF16) return run_chain<__nv_bfloat16>(a, sampling);
   return SPEC_ERR_UNSUPPORTED;
+}
+
+// ---------------------------------------------------------------------------
+// top-k / top-p chain
+// ---------------------------------------------------------------------------
+struct TkLayout {
+  Layout base;  // header (status)
+  size_t list_idx, list_val, rowtk, rowd, total;
+};
+
+TkLayout tk_layout(int B, int gamma, int V) {
+  TkLayout L;
+  L.base = layout(B, gamma, V);
+  const size_t rows = static_cast<size_t>(B) * (2 * gamma + 1);
+  size_t off = L.base.total;
+  L.list_idx = off;
+  off += align_up(rows * kTkStore * sizeof(int), 256);
+  L.list_val = off;
+  off += align_up(rows * kTkStore * sizeof(float), 256);
+  L.rowtk = off;
+  off += align_up(rows * sizeof(float4), 256);
+  L.rowd = off;
+  off += align_up(rows * sizeof(float2), 256);
+  L.total = off;
+  return L;
+}
+
+template <typename T>
+int run_topkp(const Common& a, int top_k, float top_p) {
+  const TkLayout L = tk_layout(a.B, a.gamma, a.V);
+  if (a.ws_bytes < L.total) return SPEC_ERR_WORKSPACE;
+  uint8_t* ws = static_cast<uint8_t*>(a.ws);
+  TopkTailParams tp = {};
+  TopkParams& k = tp.tk;
+  k.target = a.target;
+  k.draft = a.draft;
+  k.temperature = a.temperature;
+  k.list_idx = reinterpret_cast<int*>(ws + L.list_idx);
+  k.list_val = reinterpret_cast<float*>(ws + L.list_val);
+  k.rowtk = reinterpret_cast<float4*>(ws + L.rowtk);
+  k.rowd = reinterpret_cast<float2*>(ws + L.rowd);
+  k.draft_tokens = a.draft_tokens;
+  k.status = reinterpret_cast<int*>(ws + L.base.header);
+  k.B = a.B;
+  k.gamma = a.gamma;
+  k.V = a.V;
+  k.top_k = top_k;
+  k.top_p = top_p;
+  topk_select_kernel<T><<<a.B * (2 * a.gamma + 1), kTkThreads, 0, a.stream>>>(k);
+  if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
+  DecideParams& dp = tp.dp;
+  dp.target = a.target;
+  dp.draft = a.draft;
+  dp.draft_tokens = a.draft_tokens;
+  dp.temperature = a.temperature;
+  dp.u_accept = a.u_accept;
+  dp.out_tokens = a.out_tokens;
+  dp.out_num = a.out_num;
+  dp.out_debug = a.out_debug;
+  dp.status = k.status;
+  dp.gamma = a.gamma;
+  dp.V = a.V;
+  tp.u_resample = a.u_resample;
+  if (launch_pdl(topkp_tail_kernel<T>, dim3(a.B), dim3(kTkThreads), 0, a.stream, tp) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+  return SPEC_OK;
 }
 
 // ---------------------------------------------------------------------------
@@ -688,6 +755,48 @@ int spec_verify_lmhead_gemm_only(const void* hidden, const void* W, const void* 
                       V, H, out_tokens, out_num_accepted, out_debug, workspace, workspace_bytes, stream);
 }
 
+int spec_verify_topkp_workspace_bytes(int B, int gamma, int V, size_t* bytes) {
+  if (bytes == nullptr || check_shape(B, gamma, V) != SPEC_OK) return SPEC_ERR_INVALID_ARG;
+  *bytes = tk_layout(B, gamma, V).total;
+  return SPEC_OK;
+}
+
+int spec_verify_sample_topkp(const void* target_logits, const void* draft_logits, spec_dtype dt,
+                             const int32_t* draft_tokens, const float* temperature, const float* u_accept,
+                             const float* u_resample, int B, int gamma, int V, int top_k, float top_p,
+                             int32_t* out_tokens, int32_t* out_num_accepted, float* out_debug, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  if (target_logits == nullptr || draft_logits == nullptr || draft_tokens == nullptr ||
+      temperature == nullptr || u_accept == nullptr || u_resample == nullptr || out_tokens == nullptr ||
+      out_num_accepted == nullptr)
+    return SPEC_ERR_INVALID_ARG;
+  if (int e = check_shape(B, gamma, V)) return e;
+  if (top_k < 1 || top_k > kTkMaxK || !(top_p > 0.f && top_p <= 1.f)) return SPEC_ERR_INVALID_ARG;
+  if (dt != SPEC_F32 && dt != SPEC_BF16) return SPEC_ERR_UNSUPPORTED;
+  if (!aligned16(target_logits) || !aligned16(draft_logits)) return SPEC_ERR_ALIGNMENT;
+  if (out_debug != nullptr && !aligned16(out_debug)) return SPEC_ERR_ALIGNMENT;
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return SPEC_ERR_WORKSPACE;
+  Common a = {};
+  a.target = target_logits;
+  a.draft = draft_logits;
+  a.dt = dt;
+  a.draft_tokens = draft_tokens;
+  a.temperature = temperature;
+  a.u_accept = u_accept;
+  a.u_resample = u_resample;
+  a.B = B;
+  a.gamma = gamma;
+  a.V = V;
+  a.out_tokens = out_tokens;
+  a.out_num = out_num_accepted;
+  a.out_debug = out_debug;
+  a.ws = workspace;
+  a.ws_bytes = workspace_bytes;
+  a.stream = static_cast<cudaStream_t>(stream);
+  return dt == SPEC_F32 ? run_topkp<float>(a, top_k, top_p) : run_topkp<__nv_bfloat16>(a, top_k, top_p);
+}
+
 int spec_verify_status(void* workspace, void* stream) {
   if (workspace == nullptr) return SPEC_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -697,6 +806,7 @@ int spec_verify_status(void* workspace, void* stream) {
   if (st != 0 && cudaMemset(workspace, 0, sizeof(int)) != cudaSuccess) return SPEC_ERR_CUDA;
   if (st & kStatusTimeout) return SPEC_ERR_TIMEOUT;
   if (st & kStatusBadToken) return SPEC_ERR_DEVICE_INPUT;
+  if (st & kStatusTopkOverflow) return SPEC_ERR_UNSUPPORTED;
   return SPEC_OK;
 }
 

@@ -201,3 +201,37 @@ def _multi(lib, **kw):
 ])
 def test_greedy_multi_rejects_bad_arguments_on_host(lib, kw, code):
     assert _multi(lib, **kw) == code
+
+
+def _topkp(lib, **kw):
+    args = dict(t=A16, d=A16, dt=sv.SPEC_BF16, tok=A16, temp=A16, ua=A16, ur=A16, B=4, g=4, V=4096, k=64,
+                p=0.95, out=A16, num=A16, dbg=None, ws=WS, wsb=1 << 30)
+    args.update(kw)
+    return lib.spec_verify_sample_topkp(args["t"], args["d"], args["dt"], args["tok"], args["temp"], args["ua"],
+                                        args["ur"], args["B"], args["g"], args["V"], args["k"], args["p"],
+                                        args["out"], args["num"], args["dbg"], args["ws"], args["wsb"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(t=None), sv.SPEC_ERR_INVALID_ARG),
+    (dict(ur=None), sv.SPEC_ERR_INVALID_ARG),
+    (dict(k=0), sv.SPEC_ERR_INVALID_ARG),
+    (dict(k=1025), sv.SPEC_ERR_INVALID_ARG),
+    (dict(p=0.0), sv.SPEC_ERR_INVALID_ARG),
+    (dict(p=1.5), sv.SPEC_ERR_INVALID_ARG),
+    (dict(p=float("nan")), sv.SPEC_ERR_INVALID_ARG),
+    (dict(V=4100), sv.SPEC_ERR_INVALID_ARG),
+    (dict(dt=3), sv.SPEC_ERR_UNSUPPORTED),
+    (dict(d=A8), sv.SPEC_ERR_ALIGNMENT),
+    (dict(ws=WS + 8), sv.SPEC_ERR_WORKSPACE),
+    (dict(wsb=4096), sv.SPEC_ERR_WORKSPACE),
+])
+def test_topkp_rejects_bad_arguments_on_host(lib, kw, code):
+    assert _topkp(lib, **kw) == code
+
+
+def test_topkp_workspace_bytes(lib):
+    plain = sv.spec_verify_workspace_bytes(32, 4, 262144)
+    out = ctypes.c_size_t(0)
+    assert lib.spec_verify_topkp_workspace_bytes(32, 4, 262144, ctypes.byref(out)) == sv.SPEC_OK
+    assert out.value >= plain + 32 * 9 * 2048 * 8      # the kept lists

@@ -647,3 +647,119 @@ def test_round_update_gamma_schedule_and_errors():
     bad = oracle.RoundState(gamma=4, seq_len=7, kv_len=7)
     with pytest.raises(ValueError):
         oracle.round_update(bad, 1, 1, 10)         # cache and sequence disagree
+
+
+# ---------------------------------------------------------------------------
+# top-k / top-p truncation ("Gemma 4 MTP 深度解析" §5.1: top_k=64, top_p=0.95;
+# "第 8 章…" 为什么输出不会变: target and draft transformed the same way)
+# ---------------------------------------------------------------------------
+def _hf_truncate(l, T, k, top_p):
+    """An independent formulation for distinct logits: keep the k largest
+    scores; sort ascending, drop tokens whose cumulative softmax is <= 1 -
+    top_p (the largest always stays); softmax of what is left."""
+    z = np.asarray(l, np.float64) / T
+    kth = np.sort(z)[::-1][min(k, len(z)) - 1]
+    z = np.where(z < kth, -np.inf, z)
+    order = np.argsort(z)
+    pz = scipy.special.softmax(z[order])
+    drop = np.cumsum(pz) <= 1 - top_p
+    drop[-1] = False
+    zz = z.copy()
+    zz[order[drop]] = -np.inf
+    return scipy.special.softmax(zz)
+
+
+def test_truncate_topk_counts_and_ties():
+    rng = np.random.default_rng(43)
+    l = rng.normal(0, 2, 200)
+    for k in (1, 5, 64, 199, 200, 500):
+        p, _ = so.truncate_probs(l, 1.0, k, 1.0)
+        assert (p > 0).sum() == min(k, 200)
+        top = np.argsort(-l)[:min(k, 200)]
+        assert set(np.flatnonzero(p)) == set(top)
+    p, _ = so.truncate_probs(np.array([3.0, 1.0, 1.0, 1.0, 0.0]), 1.0, 2, 1.0)
+    assert list(p > 0) == [True, True, True, True, False]     # the tie at the 2nd value stays
+    assert abs(p.sum() - 1.0) < 1e-15
+
+
+def test_truncate_topp_dyadic_boundaries():
+    l = np.log([0.5, 0.25, 0.125, 0.125])                     # exact masses
+    keep = lambda tp: list(so.truncate_probs(l, 1.0, 10, tp)[0] > 0)
+    assert keep(0.5) == [True, False, False, False]           # mass above 0.25 is 0.5: not < 0.5
+    assert keep(0.51) == [True, True, False, False]
+    assert keep(0.75) == [True, True, False, False]           # mass above the 0.125s is 0.75
+    assert keep(0.76) == [True, True, True, True]             # the tie group enters together
+    assert keep(1e-9) == [True, False, False, False]          # the most likely token always stays
+    p, m = so.truncate_probs(l, 1.0, 10, 0.75)
+    assert abs(p[0] - 2 / 3) < 1e-15 and abs(m) < 1e-15       # the cut sits exactly on 0.75
+
+
+def test_truncate_matches_an_independent_formulation():
+    rng = np.random.default_rng(47)
+    for _ in range(300):
+        V = int(rng.integers(2, 300))
+        l = rng.normal(0, float(rng.uniform(0.3, 4)), V)
+        T = float(rng.uniform(0.3, 1.5))
+        k = int(rng.integers(1, V + 5))
+        tp = float(rng.uniform(0.05, 1.0))
+        p, m = so.truncate_probs(l, T, k, tp)
+        if m < 1e-9:
+            continue
+        assert np.allclose(p, _hf_truncate(l, T, k, tp), rtol=0, atol=1e-12)
+
+
+def test_truncation_depends_on_temperature():
+    l = np.log([0.5, 0.25, 0.125, 0.125])
+    hot, _ = so.truncate_probs(l, 2.0, 10, 0.75)               # flatter: more tokens needed
+    cold, _ = so.truncate_probs(l, 1.0, 10, 0.75)
+    assert (hot > 0).sum() > (cold > 0).sum()
+
+
+def _truncated_module(k, tp):
+    import types
+    m = types.SimpleNamespace()
+    m.row_probs = lambda logits, T: so.truncate_probs(logits, T, k, tp)[0]
+    m.acceptance_probability = so.acceptance_probability
+    m.residual_weights = so.residual_weights
+    return m
+
+
+@pytest.mark.parametrize("k,tp", [(3, 1.0), (8, 0.7), (4, 0.9)])
+def test_truncated_verification_is_lossless_V8(k, tp):
+    """With p and q truncated the same way, the emitted tokens follow the
+    truncated target distribution exactly (enumeration, V=8, gamma=2)."""
+    mod = _truncated_module(k, tp)
+    lm = ToyLM(V=8, salt=5, sd=1.2, draft_noise=1.0)
+    T = 0.9
+
+    @lru_cache(maxsize=None)
+    def first_k(prefix, kk):
+        out = {}
+        for seq, w in _round_distribution(lm, list(prefix), 2, T, mod).items():
+            if len(seq) >= kk:
+                out[seq[:kk]] = out.get(seq[:kk], 0.0) + w
+            else:
+                for rest, w2 in first_k(prefix + seq, kk - len(seq)).items():
+                    out[seq + rest] = out.get(seq + rest, 0.0) + w * w2
+        return out
+
+    spec = first_k((1,), 3)
+    err = 0.0
+    for t1 in range(8):
+        p1 = _hf_truncate(lm.target_logits([1]), T, k, tp)[t1]
+        for t2 in range(8):
+            p2 = _hf_truncate(lm.target_logits([1, t1]), T, k, tp)[t2]
+            for t3 in range(8):
+                p3 = _hf_truncate(lm.target_logits([1, t1, t2]), T, k, tp)[t3]
+                err = max(err, abs(spec.get((t1, t2, t3), 0.0) - p1 * p2 * p3))
+    assert err < 1e-12
+
+
+def test_mutation_topp_non_strict_is_caught(monkeypatch):
+    orig = so.truncate_probs
+
+    def non_strict(logits, temperature, top_k, top_p):
+        return orig(logits, temperature, top_k, np.nextafter(top_p, 2.0))  # keeps "== top_p" too
+    monkeypatch.setattr(so, "truncate_probs", non_strict)
+    with pytest.raises(AssertionError):
+        test_truncate_topp_dyadic_boundaries()
