@@ -267,12 +267,12 @@ struct SmemMass {
 // those sums finds the first thread whose prefix passes u*Z minus the mass of
 // the earlier chunks, and that thread walks its own entries.
 template <typename T>
-__device__ __noinline__ void draw_token(const SampleParams& p, int b, const SeqState s, const RowStat* rs) {
+__device__ __forceinline__ void draw_token(const SampleParams& p, int b, const SeqState s, const RowStat* rs, float u) {
   constexpr int P = Elt<T>::kPerVec;
   __shared__ float sm_mass[kTailSmemChunks];
   __shared__ F2 s_wtot[kTailWarps];
   __shared__ F2 s_local;
-  __shared__ int s_chunk, s_resid, s_first, s_tok, s_lastnz;
+  __shared__ int s_chunk, s_resid, s_first, s_lastnz;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = p.gamma, slots = 2 * g + 1;
   float* mass = p.mass + static_cast<size_t>(b) * p.cpr;
@@ -299,7 +299,7 @@ __device__ __noinline__ void draw_token(const SampleParams& p, int b, const SeqS
         ms = scan_masses_fn(sm, p.cpr);
         residual = false;  // weights of target row n as a plain row
       }
-      chunk = pick_chunk_fn(sm, ms, f2_mul_f(ms.Z, p.u_resample[b]), &local);
+      chunk = pick_chunk_fn(sm, ms, f2_mul_f(ms.Z, u), &local);
     } else {
       MassScan ms = scan_masses(mass, p.cpr);
       if (residual && !(ms.Z.hi > 0.f)) {
@@ -307,7 +307,7 @@ __device__ __noinline__ void draw_token(const SampleParams& p, int b, const SeqS
         ms = scan_masses(mass, p.cpr);
         residual = false;
       }
-      chunk = pick_chunk(mass, ms, f2_mul_f(ms.Z, p.u_resample[b]), &local);
+      chunk = pick_chunk(mass, ms, f2_mul_f(ms.Z, u), &local);
     }
     if (lane == 0) {
       s_chunk = chunk;
@@ -351,15 +351,20 @@ __device__ __noinline__ void draw_token(const SampleParams& p, int b, const SeqS
   F2 incl = warp_scan_incl(my);
   if (lane == 31) s_wtot[warp] = incl;
   __syncthreads();
-  F2 wpre = f2_from(0.f);
-  for (int w2 = 0; w2 < warp; ++w2) wpre = f2_add(wpre, s_wtot[w2]);
-  incl = f2_add(incl, wpre);
+  // prefix of the earlier warps' totals: every warp scans the kTailWarps
+  // totals (one per lane) at once instead of adding them one by one
+  F2 wt = (lane < kTailWarps) ? s_wtot[lane] : f2_from(0.f);
+  wt = warp_scan_incl(wt);
+  const F2 wpre = f2_shfl(wt, warp > 0 ? warp - 1 : 0);
+  if (warp > 0) incl = f2_add(incl, wpre);
   // the prefix sums are non-decreasing in t: the first thread whose inclusive
   // prefix passes `local` holds the entry
   if (f2_gt(incl, local)) atomicMin(&s_first, t);
   if (last_nz >= 0) atomicMax(&s_lastnz, last_nz);
   __syncthreads();
-  if (t == s_first) {
+  const int first = s_first;
+  const int out_pos = b * (g + 1) + s.n;
+  if (t == first) {
     F2 run = f2_sub(incl, my);
     int tok = -1;
 #pragma unroll
@@ -367,18 +372,16 @@ __device__ __noinline__ void draw_token(const SampleParams& p, int b, const SeqS
       run = f2_add(run, f2_from(w[k]));
       if (tok < 0 && f2_gt(run, local)) tok = t * P + k;
     }
-    s_tok = (tok >= 0) ? tok : last_nz;  // rounding inside the thread: its last nonzero entry
-  }
-  __syncthreads();
-  if (t == 0) {
+    if (tok < 0) tok = (last_nz >= 0) ? last_nz : max(s_lastnz, 0);  // rounding inside the thread
+    p.dp.out_tokens[out_pos] = chunk * p.CE + tok;
+  } else if (first == INT_MAX && t == 0) {
     // beyond the chunk total (rounding): the chunk's last nonzero entry
-    const int tok = (s_first != INT_MAX && s_tok >= 0) ? s_tok : (s_lastnz < 0 ? 0 : s_lastnz);
-    p.dp.out_tokens[b * (g + 1) + s.n] = chunk * p.CE + tok;
+    p.dp.out_tokens[out_pos] = chunk * p.CE + max(s_lastnz, 0);
   }
 }
 
 template <typename T>
-__global__ void __launch_bounds__(kTailThreads, 1) tail_kernel(const __grid_constant__ SampleParams p) {
+__global__ void __launch_bounds__(kTailThreads, 2) tail_kernel(const __grid_constant__ SampleParams p) {
   __shared__ RowStat rs[2 * 31 + 1];  // gamma <= 31
   __shared__ SeqState s_seq;
   __shared__ int s_last;
@@ -390,6 +393,7 @@ __global__ void __launch_bounds__(kTailThreads, 1) tail_kernel(const __grid_cons
   // inputs of the decision do not depend on the row reducer: load them first
   DecideIn din;
   if (warp == 0) din = prefetch_decide<T>(p.dp, b, greedy);
+  const float u_res = greedy ? 0.f : p.u_resample[b];  // an input: loaded before the wait too
   grid_dep_wait();
 
   // ---- combine the sequence's rows, one warp per row ----
@@ -431,7 +435,7 @@ __global__ void __launch_bounds__(kTailThreads, 1) tail_kernel(const __grid_cons
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  draw_token<T>(p, b, s, rs);
+  draw_token<T>(p, b, s, rs, u_res);
 }
 
 }  // namespace specv

@@ -225,10 +225,11 @@ int run_chain(const Common& a, bool sampling) {
   dp.status = status;
   dp.gamma = a.gamma;
   dp.V = a.V;
-  // parts per sequence: about one CTA per SM over the batch (at most 16), so
-  // the tail's CTAs start as soon as the row reducer frees the SMs; greedy
-  // calls need one (no residual pass)
-  int parts = sampling ? (dev.sms + a.B - 1) / a.B : 1;
+  // parts per sequence: as many CTAs as fit on the GPU at once (two per SM),
+  // at most 16, so the tail's CTAs all start as the row reducer frees the SMs
+  // (a second wave would start late) and the residual masses spread over every
+  // SM; greedy calls need one (no residual pass)
+  int parts = sampling ? (2 * dev.sms) / a.B : 1;
   if (parts > 16) parts = 16;
   if (parts > pl.cpr) parts = pl.cpr;
   if (parts < 1) parts = 1;
