@@ -267,6 +267,7 @@ __global__ void __launch_bounds__(kRowThreads, (kPath == kLdg) ? 2 : 1)
   __shared__ __align__(8) uint64_t never_bar;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   grid_dep_launch();  // let the accept kernel's launch overlap this one
+  grid_dep_wait();    // the logits and the workspace may come from the previous grid
 
   if (p.debug & 1) {  // self-test: a wait nobody can satisfy must end by itself
     if (threadIdx.x == 0) {

@@ -398,7 +398,7 @@ __global__ void __launch_bounds__(kTailThreads, 2) tail_kernel(const __grid_cons
 
   // ---- combine the sequence's rows, one warp per row ----
   for (int r = warp; r < nrows; r += kTailWarps) {
-    const RowStat st = combine_row(p.partials + static_cast<size_t>(b * slots + r) * p.cpr, p.cpr, !greedy);
+    const RowStat st = combine_row<4>(p.partials + static_cast<size_t>(b * slots + r) * p.cpr, p.cpr, !greedy);
     if (lane == 0) rs[r] = st;
   }
   __syncthreads();

@@ -194,11 +194,15 @@ int run_chain(const Common& a, bool sampling) {
   rp.CE = pl.CE;
   rp.cpr = pl.cpr;
   rp.debug = a.debug;
+  // programmatic launch: the reducer waits for the previous grid in the stream
+  // (griddepcontrol.wait) before it reads anything, so only the launch
+  // latency overlaps the predecessor's tail
+  cudaError_t e;
   if (dev.path == kTma)
-    rowstats_kernel<T, kTma><<<pl.grid, kRowThreads, pl.smem, a.stream>>>(rp);
+    e = launch_pdl(rowstats_kernel<T, kTma>, dim3(pl.grid), dim3(kRowThreads), pl.smem, a.stream, rp);
   else
-    rowstats_kernel<T, kLdg><<<pl.grid, kRowThreads, 0, a.stream>>>(rp);
-  if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
+    e = launch_pdl(rowstats_kernel<T, kLdg>, dim3(pl.grid), dim3(kRowThreads), 0, a.stream, rp);
+  if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
   if (a.debug || a.reduce_only) return SPEC_OK;
 
   SampleParams sp;
