@@ -763,3 +763,155 @@ def test_mutation_topp_non_strict_is_caught(monkeypatch):
     monkeypatch.setattr(so, "truncate_probs", non_strict)
     with pytest.raises(AssertionError):
         test_truncate_topp_dyadic_boundaries()
+
+
+# ---------------------------------------------------------------------------
+# centroid-masked sparse draft head and verification against its sparse q
+# ("Gemma 4 MTP 深度解析" §3.4 Centroids Masking; "Gemma 4 - Drafter 解析", 高效 Embedder)
+# ---------------------------------------------------------------------------
+def _brute_head(h, C, W, off, o2t, top_k):
+    """Explicit loops: fsum dot products, a Python sort by (-score, index)."""
+    out = []
+    for r in range(len(h)):
+        z = [math.fsum(float(h[r][k]) * float(C[c][k]) for k in range(len(h[r]))) for c in range(len(C))]
+        sel = sorted(range(len(C)), key=lambda c: (-z[c], c))[:top_k]
+        cand = []
+        for c in sel:
+            for i in range(int(off[c]), int(off[c + 1])):
+                cand.append((int(o2t[i]), math.fsum(float(h[r][k]) * float(W[i][k]) for k in range(len(h[r])))))
+        cand.sort()
+        out.append(cand)
+    return out
+
+
+def _tiny_centroid(seed=5, V=64, H=8, Nc=8):
+    rng = np.random.default_rng(seed)
+    cl = rng.integers(0, Nc, V)
+    o2t = np.lexsort((np.arange(V), cl))
+    off = np.concatenate([[0], np.cumsum(np.bincount(cl, minlength=Nc))])
+    W = rng.normal(0, 1, (V, H))
+    C = rng.normal(0, 1, (Nc, H))
+    h = rng.normal(0, 1, (3, H))
+    return h, C, W, off, o2t
+
+
+def test_centroid_head_matches_brute_force():
+    h, C, W, off, o2t = _tiny_centroid()
+    for top_k in (1, 3, 8):
+        got = oracle.centroid_head(h, C, W, off, o2t, top_k)
+        want = _brute_head(h, C, W, off, o2t, top_k)
+        for (tok, lg), cand in zip(got, want):
+            assert list(tok) == [t for t, _ in cand]
+            assert np.allclose(lg, [x for _, x in cand], rtol=0, atol=1e-12)
+
+
+def test_centroid_head_all_clusters_is_the_dense_head():
+    h, C, W, off, o2t = _tiny_centroid(seed=6, V=96, H=6, Nc=7)
+    dense = oracle.lmhead_logits(h, W[np.argsort(o2t)])  # token order
+    for r, (tok, lg) in enumerate(oracle.centroid_head(h, C, W, off, o2t, 7)):
+        assert list(tok) == list(range(96))
+        assert np.allclose(lg, dense[r], rtol=0, atol=1e-12)
+
+
+def test_centroid_top_clusters_ties_keep_the_lowest_index():
+    assert list(oracle.top_clusters([1.0, 3.0, 3.0, 2.0, 3.0], 2)) == [1, 2]
+    assert list(oracle.top_clusters([0.5, 0.5, 0.5], 3)) == [0, 1, 2]
+    h, C, W, off, o2t = _tiny_centroid(seed=8)
+    C[5] = C[2]  # clusters 2 and 5 score the same for every row
+    z = oracle.cluster_scores(h, C)
+    for r in range(len(h)):
+        sel = list(oracle.top_clusters(z[r], 8))
+        assert sel.index(2) < sel.index(5)
+
+
+def test_sparse_row_to_dense_gives_the_candidate_softmax():
+    tok = np.array([1, 4, 6])
+    lg = np.array([0.5, -1.0, 2.0])
+    row = oracle.sparse_row_to_dense(tok, lg, 8)
+    q = oracle.row_probs(row, 0.7)
+    want = scipy.special.softmax(lg / 0.7)
+    assert np.allclose(q[tok], want, rtol=0, atol=1e-15)
+    assert q[[0, 2, 3, 5, 7]].sum() == 0.0
+
+
+class _MaskedDraftLM(ToyLM):
+    """q restricted to the 3 tokens with the largest draft logits (q = 0 elsewhere)."""
+
+    def draft_logits(self, prefix):
+        l = super().draft_logits(prefix)
+        keep = np.argsort(-l, kind="stable")[:3]
+        tok = np.sort(keep)
+        return oracle.sparse_row_to_dense(tok, l[tok], self.V)
+
+
+def test_sparse_draft_verification_is_lossless_V8():
+    lm = _MaskedDraftLM(V=8, salt=11, sd=1.2, draft_noise=1.0)
+    T = 0.9
+
+    @lru_cache(maxsize=None)
+    def first_k(prefix, kk):
+        out = {}
+        for seq, w in _round_distribution(lm, list(prefix), 2, T, so).items():
+            if len(seq) >= kk:
+                out[seq[:kk]] = out.get(seq[:kk], 0.0) + w
+            else:
+                for rest, w2 in first_k(prefix + seq, kk - len(seq)).items():
+                    out[seq + rest] = out.get(seq + rest, 0.0) + w * w2
+        return out
+
+    spec = first_k((2,), 3)
+    err = 0.0
+    for t1 in range(8):
+        p1 = scipy.special.softmax(lm.target_logits([2]) / T)[t1]
+        for t2 in range(8):
+            p2 = scipy.special.softmax(lm.target_logits([2, t1]) / T)[t2]
+            for t3 in range(8):
+                p3 = scipy.special.softmax(lm.target_logits([2, t1, t2]) / T)[t3]
+                err = max(err, abs(spec.get((t1, t2, t3), 0.0) - p1 * p2 * p3))
+    assert err < 1e-12
+
+
+def test_verify_sample_sparse_full_candidates_is_verify_sample():
+    import workloads as wl
+    m = wl.make_centroid_model(V=2048, H=32, n_clusters=16, seed=3, mu_sd=0.3, eps_sd=0.05)
+    rd = wl.make_centroid_round(m, B=6, gamma=3, r=1, draft_sd=0.1, temperature=0.8)
+    cand = oracle.centroid_head(rd["hidden_draft"], m.centroids, m.W_ord, m.cluster_off, m.ord2tok, 16)
+    d = wl.sample_sparse_drafts(cand, rd["temperature"], 3, r=1)
+    dense = oracle.lmhead_logits(rd["hidden_draft"], m.W_ord[m.tok2ord]).reshape(6, 3, -1)
+    got = oracle.verify_sample_sparse(rd["target"], [[cand[b * 3 + j] for j in range(3)] for b in range(6)], d,
+                                      rd["temperature"], rd["u_accept"], rd["u_resample"])
+    want = oracle.verify_sample(rd["target"], dense, d, rd["temperature"], rd["u_accept"], rd["u_resample"])
+    for a, b in zip(got, want):
+        assert a.n == b.n and a.tokens == b.tokens
+
+
+def test_mutation_centroid_rules_are_caught(monkeypatch):
+    """Highest index on ties, or a cluster range one row short, fails a pin."""
+    import oracle.centroid as oc
+    orig_top = oc.top_clusters
+    highest = lambda s, k: np.lexsort((-np.arange(len(s)), -np.asarray(s)))[:k]
+    monkeypatch.setattr(oc, "top_clusters", highest)
+    monkeypatch.setattr(oracle, "top_clusters", highest)
+    with pytest.raises(AssertionError):
+        test_centroid_top_clusters_ties_keep_the_lowest_index()
+    monkeypatch.setattr(oc, "top_clusters", orig_top)
+    monkeypatch.setattr(oracle, "top_clusters", orig_top)
+    orig_head = oc.centroid_head
+
+    def short_range(hidden, centroids, W_ord, cluster_off, ord2tok, top_k):
+        off = np.asarray(cluster_off).copy()
+        off[1:] = np.maximum(off[1:] - 1, off[:-1])
+        return orig_head(hidden, centroids, W_ord, off, ord2tok, top_k)
+    monkeypatch.setattr(oracle, "centroid_head", short_range)
+    with pytest.raises(AssertionError):
+        test_centroid_head_matches_brute_force()
+
+
+def test_mutation_sparse_fill_is_caught(monkeypatch):
+    """Non-candidates filled with logit 0 instead of -inf gives q > 0 off the
+    candidates: the softmax pin fails."""
+    orig = oracle.sparse_row_to_dense
+    monkeypatch.setattr(oracle, "sparse_row_to_dense",
+                        lambda t, l, V: np.where(np.isin(np.arange(V), t), orig(t, l, V), 0.0))
+    with pytest.raises(AssertionError):
+        test_sparse_row_to_dense_gives_the_candidate_softmax()

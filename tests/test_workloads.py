@@ -70,3 +70,30 @@ def test_lmhead_exact_sums_recipe_is_exact_in_fp32_any_order():
     # the realistic recipe is not on the grid
     inp2 = wl.make_lmhead_round(0, B=B, gamma=gamma, V=V, H=H)
     assert np.any(np.rint(wl.bf16_bits_to_f32(inp2.hidden) * 8) != wl.bf16_bits_to_f32(inp2.hidden) * 8)
+
+
+def test_centroid_exact_sums_recipe_is_on_the_grid_and_exact():
+    """Exact-sums centroid recipe: embeddings and centroids on the 2^-11 grid
+    (|k| <= 255), hidden states on the 1/8 grid (|k| <= 32); fp32 sums of the
+    products in any order equal the float64 dot products."""
+    m = wl.make_centroid_model(V=512, H=1536, n_clusters=16, seed=2, exact_sums=True)
+    rd = wl.make_centroid_round(m, B=2, gamma=2, exact_sums=True)
+    w = wl.bf16_bits_to_f32(m.W_ord)
+    c = wl.bf16_bits_to_f32(m.centroids)
+    h = wl.bf16_bits_to_f32(rd["hidden_draft"])
+    for a in (w, c):
+        assert np.all(np.abs(a) <= 255 / 2048) and np.all(np.rint(a * 2048) == a * 2048)
+    assert np.all(np.abs(h) <= 4) and np.all(np.rint(h * 8) == h * 8)
+    rng = np.random.default_rng(9)
+    for mat in (w[::37], c):
+        exact = h.astype(np.float64) @ mat.astype(np.float64).T
+        for r in range(h.shape[0]):
+            for x in range(mat.shape[0]):
+                prod = (h[r] * mat[x]).astype(np.float32)
+                acc = np.float32(0)
+                for t in prod[rng.permutation(prod.size)]:
+                    acc = np.float32(acc + t)
+                assert float(acc) == exact[r, x]
+    # cluster layout: ordered rows are grouped by cluster, ord2tok / tok2ord invert each other
+    assert m.cluster_off[0] == 0 and m.cluster_off[-1] == m.V and np.all(np.diff(m.cluster_off) >= 0)
+    assert np.array_equal(m.tok2ord[m.ord2tok], np.arange(m.V))
