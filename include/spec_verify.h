@@ -181,6 +181,70 @@ int spec_verify_sample_topkp(const void *target_logits, const void *draft_logits
                              void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Centroid-masked sparse draft head ("Gemma 4 Multi-Token Prediction (MTP)
+ * 深度解析" §3.4 Centroids Masking; "Gemma 4 - Drafter 解析", 高效 Embedder).
+ * The token embeddings are stored cluster by cluster: cluster c owns the
+ * ordered rows cluster_off[c] .. cluster_off[c+1]-1 of W_ord, and ordered row
+ * i is token ord2tok[i].  For each of the R hidden rows h (the drafter's
+ * hidden state at one draft position):
+ *   z[c]  = h . centroids[c]                 (fp32 sums of bf16 products)
+ *   S     = the top_k clusters by z, the lowest cluster index first among
+ *           equal scores;
+ *   out   = (token, h . W_ord[i]) for every ordered row i of the clusters in
+ *           S, ascending token id; out_count[r] candidates.
+ * Tokens outside S get no logit: the draft distribution is the softmax over
+ * the candidates (spec_verify_sample_sparse consumes exactly this layout).
+ *
+ * Layouts (device, row-major): hidden [R, H], centroids [n_clusters, H],
+ * W_ord [V, H] bf16, 16-byte aligned, 256 <= H <= 4096, H % 256 == 0;
+ * cluster_off int32 [n_clusters+1] (non-decreasing, 0 .. V); ord2tok int32
+ * [V] (a permutation of 0..V-1); out_tok int32 and out_logit f32
+ * [R, max_cand]; out_count int32 [R].  1 <= n_clusters <= 8192,
+ * 1 <= top_k <= min(n_clusters, 256), 1 <= max_cand <= 8192.  A row whose
+ * clusters hold more than max_cand tokens keeps the first max_cand (in
+ * cluster-score order) and makes spec_verify_status return
+ * SPEC_ERR_UNSUPPORTED.  The workspace (spec_centroid_head_workspace_bytes,
+ * zeroed once by spec_verify_workspace_init) holds the scores, the selection
+ * and the status word.  Asynchronous; host checks return negative codes.
+ */
+int spec_centroid_head_workspace_bytes(int R, int n_clusters, int top_k, size_t *bytes);
+
+int spec_centroid_head(const void *hidden, const void *centroids, const void *W_ord,
+                       const int32_t *cluster_off, const int32_t *ord2tok, int R, int H, int V,
+                       int n_clusters, int top_k, int max_cand, int32_t *out_tok,
+                       float *out_logit, int32_t *out_count, void *workspace,
+                       size_t workspace_bytes, void *stream);
+
+/*
+ * Rejection-sampling verification against sparse draft rows.  Draft row j of
+ * sequence b (row b*gamma + j of the candidate arrays) is cand_count[row]
+ * candidates: tokens cand_tok[row*cand_stride + i] in ascending order, with
+ * logits cand_logit[row*cand_stride + i] (the layout spec_centroid_head
+ * writes).  q_j = softmax(logits / T) over the candidates and 0 elsewhere; the
+ * rule is spec_verify_sample's ("Gemma 4 Multi-Token Prediction (MTP) 深度解析"
+ * §2.2): accept iff u_accept < p(d)/q(d), a draft that is not a candidate
+ * (q(d) = 0) is accepted; after a rejection at n the token is drawn from
+ * max(0, p_n - q_n), which is p_n itself on every non-candidate token; after
+ * a full acceptance the bonus is drawn from p_gamma.  Only the target rows are
+ * streamed.  out_debug's L_q is the normaliser over the candidates.
+ *
+ * target_logits [B, gamma+1, V] f32 or bf16 (16-byte aligned, V % 8 == 0);
+ * cand_stride >= 1; counts outside [0, cand_stride] are clamped.  Other
+ * arguments, ownership and errors as spec_verify_sample; the workspace comes
+ * from spec_verify_sparse_workspace_bytes.
+ */
+int spec_verify_sparse_workspace_bytes(int B, int gamma, int V, size_t *bytes);
+
+int spec_verify_sample_sparse(const void *target_logits, spec_dtype dt, const int32_t *cand_tok,
+                              const float *cand_logit, const int32_t *cand_count,
+                              int cand_stride, const int32_t *draft_tokens,
+                              const float *temperature, const float *u_accept,
+                              const float *u_resample, int B, int gamma, int V,
+                              int32_t *out_tokens, int32_t *out_num_accepted,
+                              float *out_debug, void *workspace, size_t workspace_bytes,
+                              void *stream);
+
+/*
  * Timing / profiling aid: the same arguments and checks as
  * spec_verify_sample, but only the first kernel of its launch chain (the
  * vocab-row reducer, which streams every logit the call reads) is enqueued,

@@ -25,7 +25,7 @@ from __future__ import annotations
 
 import numpy as np
 
-from .spec_oracle import _as_f64, verify_sample_seq
+from .spec_oracle import _as_f64, _decide_and_draw, row_log_normaliser, verify_greedy_seq
 
 __all__ = ["cluster_scores", "top_clusters", "centroid_head", "sparse_row_to_dense",
            "verify_sample_sparse"]
@@ -82,16 +82,34 @@ def verify_sample_sparse(target, cand, draft_tokens, temperature, u_accept, u_re
 
     target [B, gamma+1, V]; cand[b][j] = (tokens, logits) of draft row j of
     sequence b.  q_j is the softmax of the candidates' logits / T and 0 off the
-    candidates; the rest is ``verify_sample_seq`` unchanged (accept iff
-    u < p/q, q(d) = 0 accepting; the residual max(0, p - q) puts p's own mass
-    on every non-candidate token).
+    candidates (a row without candidates is q = 0 everywhere).  The rule is
+    the dense one ([MTP-deep] §2.2; [Self-spec] §3.2): accept iff
+    u < p(d)/q(d), q(d) = 0 accepting; after a rejection at n draw from
+    max(0, p_n - q_n), which is p_n itself on every non-candidate token; after
+    a full acceptance draw the bonus from p_gamma.
     """
     B = len(draft_tokens)
     idx = range(B) if seqs is None else seqs
     out = []
     for b in idx:
-        V = np.asarray(target[b]).shape[-1]
-        rows = np.stack([sparse_row_to_dense(t, l, V) for (t, l) in cand[b]])
-        out.append(verify_sample_seq(target[b], rows, draft_tokens[b], temperature[b],
-                                     u_accept[b], u_resample[b]))
+        T = float(temperature[b])
+        if T <= 0.0:
+            out.append(verify_greedy_seq(target[b], draft_tokens[b]))
+            continue
+        tp = _as_f64(target[b])
+        V = tp.shape[-1]
+        d = [int(x) for x in draft_tokens[b]]
+        gamma = len(d)
+        L_p = [row_log_normaliser(tp[j], T) for j in range(gamma + 1)]
+        P = [np.exp(tp[j] / T - L_p[j]) for j in range(gamma + 1)]
+        Q, L_q = [], []
+        for (tok, lg) in cand[b]:
+            if len(tok) == 0:
+                Q.append(np.zeros(V))
+                L_q.append(-np.inf)
+                continue
+            row = sparse_row_to_dense(tok, lg, V)
+            L_q.append(row_log_normaliser(row, T))
+            Q.append(np.exp(row / T - L_q[-1]))
+        out.append(_decide_and_draw(P, Q, d, u_accept[b], u_resample[b], L_p, L_q))
     return out

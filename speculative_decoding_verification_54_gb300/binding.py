@@ -31,7 +31,8 @@ EXPORTED = (
     "spec_verify_version", "spec_verify_selftest_timeout", "spec_verify_sample_reduce_only",
     "spec_verify_sample_noalloc", "spec_verify_lmhead_sample", "spec_verify_lmhead_gemm_only",
     "spec_verify_greedy_multi", "spec_round_update", "spec_verify_topkp_workspace_bytes",
-    "spec_verify_sample_topkp",
+    "spec_verify_sample_topkp", "spec_centroid_head_workspace_bytes", "spec_centroid_head",
+    "spec_verify_sparse_workspace_bytes", "spec_verify_sample_sparse",
 )
 
 
@@ -74,6 +75,12 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.spec_verify_topkp_workspace_bytes.argtypes = [_i, _i, _i, ctypes.POINTER(_sz)]
     lib.spec_verify_sample_topkp.argtypes = [_vp, _vp, _i, _vp, _vp, _vp, _vp, _i, _i, _i, _i, ctypes.c_float,
                                              _vp, _vp, _vp, _vp, _sz, _vp]
+    lib.spec_centroid_head_workspace_bytes.argtypes = [_i, _i, _i, ctypes.POINTER(_sz)]
+    lib.spec_centroid_head.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp,
+                                       _vp, _sz, _vp]
+    lib.spec_verify_sparse_workspace_bytes.argtypes = [_i, _i, _i, ctypes.POINTER(_sz)]
+    lib.spec_verify_sample_sparse.argtypes = [_vp, _i, _vp, _vp, _vp, _i, _vp, _vp, _vp, _vp, _i, _i, _i,
+                                              _vp, _vp, _vp, _vp, _sz, _vp]
     lib.spec_verify_status.argtypes = [_vp, _vp]
     lib.spec_verify_error_string.argtypes = [_i]
     lib.spec_verify_error_string.restype = ctypes.c_char_p
@@ -326,3 +333,66 @@ def spec_verify_version() -> int:
 def spec_verify_selftest_timeout(workspace, stream=None) -> None:
     _check(load().spec_verify_selftest_timeout(_ptr(workspace), _nbytes(workspace), _stream(stream)),
            "spec_verify_selftest_timeout")
+
+
+# ---------------------------------------------------------------------------
+# centroid-masked sparse draft head and verification against its sparse rows
+# ---------------------------------------------------------------------------
+def _aligned_zeros(n: int, device):
+    import torch
+    ws = torch.zeros(n + 256, dtype=torch.uint8, device=device)
+    off = (-ws.data_ptr()) % 256
+    return ws[off:off + n]
+
+
+def spec_centroid_head_workspace_bytes(R: int, n_clusters: int, top_k: int) -> int:
+    out = _sz(0)
+    _check(load().spec_centroid_head_workspace_bytes(R, n_clusters, top_k, ctypes.byref(out)),
+           "spec_centroid_head_workspace_bytes")
+    return out.value
+
+
+def make_centroid_head_workspace(R: int, n_clusters: int, top_k: int, device="cuda"):
+    """Allocate (torch) and zero a workspace for spec_centroid_head."""
+    return _aligned_zeros(spec_centroid_head_workspace_bytes(R, n_clusters, top_k), device)
+
+
+def spec_centroid_head(hidden, centroids, W_ord, cluster_off, ord2tok, top_k, out_tok, out_logit,
+                       out_count, workspace, stream=None) -> None:
+    """hidden [R, H], centroids [n_clusters, H], W_ord [V, H] (bf16); cluster_off
+    int32 [n_clusters+1]; ord2tok int32 [V]; out_tok int32 / out_logit f32
+    [R, max_cand]; out_count int32 [R]."""
+    R, H = hidden.shape
+    V = W_ord.shape[0]
+    n_clusters = centroids.shape[0]
+    max_cand = out_tok.shape[1]
+    _check(load().spec_centroid_head(
+        _ptr(hidden), _ptr(centroids), _ptr(W_ord), _ptr(cluster_off), _ptr(ord2tok), R, H, V, n_clusters,
+        int(top_k), max_cand, _ptr(out_tok), _ptr(out_logit), _ptr(out_count), _ptr(workspace),
+        _nbytes(workspace), _stream(stream)), "spec_centroid_head")
+
+
+def spec_verify_sparse_workspace_bytes(B: int, gamma: int, V: int) -> int:
+    out = _sz(0)
+    _check(load().spec_verify_sparse_workspace_bytes(B, gamma, V, ctypes.byref(out)),
+           "spec_verify_sparse_workspace_bytes")
+    return out.value
+
+
+def make_sparse_workspace(B: int, gamma: int, V: int, device="cuda"):
+    """Allocate (torch) and zero a workspace for spec_verify_sample_sparse."""
+    return _aligned_zeros(spec_verify_sparse_workspace_bytes(B, gamma, V), device)
+
+
+def spec_verify_sample_sparse(target_logits, cand_tok, cand_logit, cand_count, draft_tokens, temperature,
+                              u_accept, u_resample, out_tokens, out_num_accepted, workspace, out_debug=None,
+                              stream=None) -> None:
+    """target_logits [B, gamma+1, V] (fp32/bf16); cand_tok int32 / cand_logit
+    f32 [B*gamma, stride] (tokens ascending per row); cand_count int32
+    [B*gamma]; the rest as spec_verify_sample."""
+    B, g1, V = target_logits.shape
+    _check(load().spec_verify_sample_sparse(
+        _ptr(target_logits), _dtype_code(target_logits), _ptr(cand_tok), _ptr(cand_logit), _ptr(cand_count),
+        cand_tok.shape[1], _ptr(draft_tokens), _ptr(temperature), _ptr(u_accept), _ptr(u_resample), B, g1 - 1, V,
+        _ptr(out_tokens), _ptr(out_num_accepted), _ptr(out_debug), _ptr(workspace), _nbytes(workspace),
+        _stream(stream)), "spec_verify_sample_sparse")

@@ -17,6 +17,7 @@ namespace specv {
 constexpr int kStatusTimeout = 1;
 constexpr int kStatusBadToken = 2;
 constexpr int kStatusTopkOverflow = 4;  // more tied entries than a truncation list holds
+constexpr int kStatusLimit = 8;         // more candidates than the caller's capacity (centroid head)
 
 // wait limits in SM clock cycles (~2 GHz): about one second normally
 constexpr long long kWaitLimitCycles = 2000000000LL;

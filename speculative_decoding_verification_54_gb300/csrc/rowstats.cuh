@@ -58,7 +58,7 @@ enum LoadPath { kLdg = 0, kTma = 1 };
 
 struct RowStatsParams {
   const void* target;        // [B, gamma+1, V]
-  const void* draft;         // [B, gamma, V] or nullptr (greedy entry point)
+  const void* draft;         // [B, gamma, V] or nullptr (no dense draft rows: greedy or sparse drafts)
   const float* temperature;  // [B] or nullptr (every sequence greedy)
   float4* partials;          // [B*(2*gamma+1)*cpr] {M, s, argmax bits, mk}
   int* status;
@@ -70,9 +70,9 @@ struct RowStatsParams {
 // Row slot t of sequence b: t <= gamma is target row t, t > gamma is draft row
 // t-gamma-1.
 __device__ __forceinline__ int row_mode(const RowStatsParams& p, int b, int t) {
-  const bool greedy = (p.draft == nullptr) || seq_is_greedy(p.temperature, b);
+  const bool greedy = (p.temperature == nullptr) || seq_is_greedy(p.temperature, b);
   if (t <= p.gamma) return p.draft_only ? kRowSkip : (greedy ? kRowArgmax : kRowFull);
-  return greedy ? kRowSkip : kRowFull;
+  return (greedy || p.draft == nullptr) ? kRowSkip : kRowFull;
 }
 
 template <typename T>

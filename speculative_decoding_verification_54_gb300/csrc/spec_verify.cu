@@ -20,12 +20,14 @@
 #include <cstring>
 #include <mutex>
 
+#include "centroid.cuh"
 #include "common.cuh"
 #include "decide.cuh"
 #include "lmhead.cuh"
 #include "lmtail.cuh"
 #include "rowstats.cuh"
 #include "sample.cuh"
+#include "sparse.cuh"
 #include "spec_verify.h"
 #include "tc.cuh"
 #include "topkp.cuh"
@@ -68,6 +70,13 @@ int device_info(DeviceInfo* out) {
     d.lm_max_dyn = optin - static_cast<int>(fa.sharedSizeBytes);
     if (cudaFuncSetAttribute(lmhead_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, d.lm_max_dyn) !=
         cudaSuccess)
+      return SPEC_ERR_CUDA;
+    // the centroid head sorts up to kHeadMaxClusters / kHeadMaxCand keys of 8 B in shared memory
+    const int sort_smem = kHeadMaxCand * static_cast<int>(sizeof(unsigned long long));
+    if (cudaFuncSetAttribute(cluster_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, sort_smem) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(cand_sort_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, sort_smem) !=
+            cudaSuccess)
       return SPEC_ERR_CUDA;
     const char* env = std::getenv("SPECV_ROW_LOADS");
     d.path = (env != nullptr && std::strcmp(env, "tma") == 0) ? kTma : kLdg;
@@ -544,6 +553,115 @@ int run_lm_chain(const LmArgs& a) {
 
 }  // namespace
 
+// ---------------------------------------------------------------------------
+// centroid-masked draft head and verification against its sparse rows
+// ---------------------------------------------------------------------------
+struct HeadLayout {
+  size_t header, scores, sel, pos, total;
+};
+
+HeadLayout head_layout(int R, int n_clusters, int top_k) {
+  HeadLayout L;
+  size_t off = 0;
+  L.header = off;
+  off += align_up(sizeof(WsHeader), 256);
+  L.scores = off;
+  off += align_up(static_cast<size_t>(R) * n_clusters * sizeof(float), 256);
+  L.sel = off;
+  off += align_up(static_cast<size_t>(R) * top_k * sizeof(int32_t), 256);
+  L.pos = off;
+  off += align_up(static_cast<size_t>(R) * (top_k + 1) * sizeof(int32_t), 256);
+  L.total = off;
+  return L;
+}
+
+int pow2_at_least(int n) {
+  int p2 = 1;
+  while (p2 < n) p2 <<= 1;
+  return p2;
+}
+
+struct SparseLayout {
+  Layout base;
+  size_t cand_lo, total;
+};
+
+SparseLayout sparse_layout(int B, int gamma, int V) {
+  SparseLayout L;
+  L.base = layout(B, gamma, V);
+  const size_t cpr = (static_cast<size_t>(V) + kMinChunk - 1) / kMinChunk;
+  L.cand_lo = L.base.total;
+  L.total = L.cand_lo + align_up(static_cast<size_t>(B) * (cpr + 1) * sizeof(int32_t), 256);
+  return L;
+}
+
+struct SparseArgs {
+  const int32_t* cand_tok;
+  const float* cand_logit;
+  const int32_t* cand_count;
+  int stride;
+};
+
+template <typename T>
+int run_sparse(const Common& a, const SparseArgs& c) {
+  const SparseLayout L = sparse_layout(a.B, a.gamma, a.V);
+  if (a.ws_bytes < L.total) return SPEC_ERR_WORKSPACE;
+  DeviceInfo dev;
+  if (device_info(&dev) != SPEC_OK) return SPEC_ERR_CUDA;
+  uint8_t* ws = static_cast<uint8_t*>(a.ws);
+  int* status = reinterpret_cast<int*>(ws + L.base.header);
+  const Plan pl = make_plan(a.B, a.gamma, a.V, sizeof(T), dev.sms, true, kLdg);
+  RowStatsParams rp = {};
+  rp.target = a.target;
+  rp.draft = nullptr;  // the draft rows are sparse: never streamed
+  rp.temperature = a.temperature;
+  rp.partials = reinterpret_cast<float4*>(ws + L.base.partials);
+  rp.status = status;
+  rp.B = a.B;
+  rp.gamma = a.gamma;
+  rp.V = a.V;
+  rp.CE = pl.CE;
+  rp.cpr = pl.cpr;
+  if (launch_pdl(rowstats_kernel<T, kLdg>, dim3(pl.grid), dim3(kRowThreads), 0, a.stream, rp) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+  SparseParams sp = {};
+  sp.target = a.target;
+  sp.cand_tok = c.cand_tok;
+  sp.cand_logit = c.cand_logit;
+  sp.cand_count = c.cand_count;
+  sp.u_resample = a.u_resample;
+  sp.partials = rp.partials;
+  sp.mass = reinterpret_cast<float*>(ws + L.base.mass);
+  sp.cand_lo = reinterpret_cast<int32_t*>(ws + L.cand_lo);
+  sp.tail_done = reinterpret_cast<int*>(ws + L.base.tail_done);
+  sp.B = a.B;
+  sp.gamma = a.gamma;
+  sp.V = a.V;
+  sp.CE = pl.CE;
+  sp.cpr = pl.cpr;
+  sp.stride = c.stride;
+  DecideParams& dp = sp.dp;
+  dp.target = a.target;
+  dp.draft = nullptr;
+  dp.draft_tokens = a.draft_tokens;
+  dp.temperature = a.temperature;
+  dp.u_accept = a.u_accept;
+  dp.out_tokens = a.out_tokens;
+  dp.out_num = a.out_num;
+  dp.out_debug = a.out_debug;
+  dp.status = status;
+  dp.gamma = a.gamma;
+  dp.V = a.V;
+  // one tail CTA per SM over the batch (at most 16 per sequence)
+  int parts = dev.sms / a.B;
+  if (parts > 16) parts = 16;
+  if (parts > pl.cpr) parts = pl.cpr;
+  if (parts < 1) parts = 1;
+  if (launch_pdl(sparse_tail_kernel<T>, dim3(parts, a.B), dim3(kSparseThreads), 0, a.stream, sp) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+  return SPEC_OK;
+}
+
 extern "C" {
 
 int spec_verify_version(void) { return 200; }
@@ -802,6 +920,105 @@ int spec_verify_sample_topkp(const void* target_logits, const void* draft_logits
   return dt == SPEC_F32 ? run_topkp<float>(a, top_k, top_p) : run_topkp<__nv_bfloat16>(a, top_k, top_p);
 }
 
+int spec_centroid_head_workspace_bytes(int R, int n_clusters, int top_k, size_t* bytes) {
+  if (bytes == nullptr || R < 1 || R > 65535 || n_clusters < 1 || n_clusters > kHeadMaxClusters || top_k < 1 ||
+      top_k > n_clusters || top_k > kHeadMaxTopK)
+    return SPEC_ERR_INVALID_ARG;
+  *bytes = head_layout(R, n_clusters, top_k).total;
+  return SPEC_OK;
+}
+
+int spec_centroid_head(const void* hidden, const void* centroids, const void* W_ord, const int32_t* cluster_off,
+                       const int32_t* ord2tok, int R, int H, int V, int n_clusters, int top_k, int max_cand,
+                       int32_t* out_tok, float* out_logit, int32_t* out_count, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  if (hidden == nullptr || centroids == nullptr || W_ord == nullptr || cluster_off == nullptr ||
+      ord2tok == nullptr || out_tok == nullptr || out_logit == nullptr || out_count == nullptr)
+    return SPEC_ERR_INVALID_ARG;
+  if (R < 1 || R > 65535 || H < 256 || H > 32 * 8 * kHeadMaxVecs || (H % 256) != 0 || V < 1 ||
+      V > SPEC_MAX_VOCAB || n_clusters < 1 || n_clusters > kHeadMaxClusters || top_k < 1 || top_k > n_clusters ||
+      top_k > kHeadMaxTopK || max_cand < 1 || max_cand > kHeadMaxCand)
+    return SPEC_ERR_INVALID_ARG;
+  if (!aligned16(hidden) || !aligned16(centroids) || !aligned16(W_ord)) return SPEC_ERR_ALIGNMENT;
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return SPEC_ERR_WORKSPACE;
+  const HeadLayout L = head_layout(R, n_clusters, top_k);
+  if (workspace_bytes < L.total) return SPEC_ERR_WORKSPACE;
+  DeviceInfo dev;
+  if (device_info(&dev) != SPEC_OK) return SPEC_ERR_CUDA;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  HeadParams hp;
+  hp.hidden = static_cast<const __nv_bfloat16*>(hidden);
+  hp.centroids = static_cast<const __nv_bfloat16*>(centroids);
+  hp.W_ord = static_cast<const __nv_bfloat16*>(W_ord);
+  hp.cluster_off = cluster_off;
+  hp.ord2tok = ord2tok;
+  hp.scores = reinterpret_cast<float*>(ws + L.scores);
+  hp.sel = reinterpret_cast<int32_t*>(ws + L.sel);
+  hp.pos = reinterpret_cast<int32_t*>(ws + L.pos);
+  hp.out_tok = out_tok;
+  hp.out_logit = out_logit;
+  hp.out_count = out_count;
+  hp.status = reinterpret_cast<int*>(ws + L.header);
+  hp.R = R;
+  hp.H = H;
+  hp.V = V;
+  hp.n_clusters = n_clusters;
+  hp.top_k = top_k;
+  hp.max_cand = max_cand;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const dim3 g1((n_clusters + kHeadWarps - 1) / kHeadWarps, (R + kHeadRowBlock - 1) / kHeadRowBlock);
+  const size_t sort1 = static_cast<size_t>(pow2_at_least(n_clusters)) * sizeof(unsigned long long);
+  const size_t sort2 = static_cast<size_t>(pow2_at_least(max_cand)) * sizeof(unsigned long long);
+  if (launch_pdl(cluster_score_kernel, g1, dim3(kHeadThreads), 0, st, hp) != cudaSuccess ||
+      launch_pdl(cluster_topk_kernel, dim3(R), dim3(kHeadThreads), sort1, st, hp) != cudaSuccess ||
+      launch_pdl(cand_logit_kernel, dim3(top_k, R), dim3(kHeadThreads), 0, st, hp) != cudaSuccess ||
+      launch_pdl(cand_sort_kernel, dim3(R), dim3(kHeadThreads), sort2, st, hp) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+  return SPEC_OK;
+}
+
+int spec_verify_sparse_workspace_bytes(int B, int gamma, int V, size_t* bytes) {
+  if (bytes == nullptr || check_shape(B, gamma, V) != SPEC_OK) return SPEC_ERR_INVALID_ARG;
+  *bytes = sparse_layout(B, gamma, V).total;
+  return SPEC_OK;
+}
+
+int spec_verify_sample_sparse(const void* target_logits, spec_dtype dt, const int32_t* cand_tok,
+                              const float* cand_logit, const int32_t* cand_count, int cand_stride,
+                              const int32_t* draft_tokens, const float* temperature, const float* u_accept,
+                              const float* u_resample, int B, int gamma, int V, int32_t* out_tokens,
+                              int32_t* out_num_accepted, float* out_debug, void* workspace, size_t workspace_bytes,
+                              void* stream) {
+  if (target_logits == nullptr || cand_tok == nullptr || cand_logit == nullptr || cand_count == nullptr ||
+      draft_tokens == nullptr || temperature == nullptr || u_accept == nullptr || u_resample == nullptr ||
+      out_tokens == nullptr || out_num_accepted == nullptr)
+    return SPEC_ERR_INVALID_ARG;
+  if (int e = check_shape(B, gamma, V)) return e;
+  if (cand_stride < 1) return SPEC_ERR_INVALID_ARG;
+  if (dt != SPEC_F32 && dt != SPEC_BF16) return SPEC_ERR_UNSUPPORTED;
+  if (!aligned16(target_logits)) return SPEC_ERR_ALIGNMENT;
+  if (out_debug != nullptr && !aligned16(out_debug)) return SPEC_ERR_ALIGNMENT;
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return SPEC_ERR_WORKSPACE;
+  Common a = {};
+  a.target = target_logits;
+  a.dt = dt;
+  a.draft_tokens = draft_tokens;
+  a.temperature = temperature;
+  a.u_accept = u_accept;
+  a.u_resample = u_resample;
+  a.B = B;
+  a.gamma = gamma;
+  a.V = V;
+  a.out_tokens = out_tokens;
+  a.out_num = out_num_accepted;
+  a.out_debug = out_debug;
+  a.ws = workspace;
+  a.ws_bytes = workspace_bytes;
+  a.stream = static_cast<cudaStream_t>(stream);
+  const SparseArgs c{cand_tok, cand_logit, cand_count, cand_stride};
+  return dt == SPEC_F32 ? run_sparse<float>(a, c) : run_sparse<__nv_bfloat16>(a, c);
+}
+
 int spec_verify_status(void* workspace, void* stream) {
   if (workspace == nullptr) return SPEC_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -811,7 +1028,7 @@ int spec_verify_status(void* workspace, void* stream) {
   if (st != 0 && cudaMemset(workspace, 0, sizeof(int)) != cudaSuccess) return SPEC_ERR_CUDA;
   if (st & kStatusTimeout) return SPEC_ERR_TIMEOUT;
   if (st & kStatusBadToken) return SPEC_ERR_DEVICE_INPUT;
-  if (st & kStatusTopkOverflow) return SPEC_ERR_UNSUPPORTED;
+  if (st & (kStatusTopkOverflow | kStatusLimit)) return SPEC_ERR_UNSUPPORTED;
   return SPEC_OK;
 }
 

@@ -22,7 +22,7 @@ def lib():
 def declared_functions():
     text = open(HEADER, encoding="utf-8").read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(spec_verify_\w+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(spec_\w+)\s*\(", text)))
 
 
 def test_header_declares_the_public_entry_points():
@@ -235,3 +235,68 @@ def test_topkp_workspace_bytes(lib):
     out = ctypes.c_size_t(0)
     assert lib.spec_verify_topkp_workspace_bytes(32, 4, 262144, ctypes.byref(out)) == sv.SPEC_OK
     assert out.value >= plain + 32 * 9 * 2048 * 8      # the kept lists
+
+
+def _head(lib, **kw):
+    args = dict(h=A16, c=A16, w=A16, off=A16, o2t=A16, R=4, H=1536, V=262144, nc=2048, k=32, mc=8192,
+                ot=A16, ol=A16, oc=A16, ws=WS, wsb=1 << 30)
+    args.update(kw)
+    return lib.spec_centroid_head(args["h"], args["c"], args["w"], args["off"], args["o2t"], args["R"], args["H"],
+                                  args["V"], args["nc"], args["k"], args["mc"], args["ot"], args["ol"], args["oc"],
+                                  args["ws"], args["wsb"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(h=None), sv.SPEC_ERR_INVALID_ARG),
+    (dict(off=None), sv.SPEC_ERR_INVALID_ARG),
+    (dict(H=1000), sv.SPEC_ERR_INVALID_ARG),
+    (dict(H=8192), sv.SPEC_ERR_INVALID_ARG),
+    (dict(nc=0), sv.SPEC_ERR_INVALID_ARG),
+    (dict(nc=8193), sv.SPEC_ERR_INVALID_ARG),
+    (dict(k=0), sv.SPEC_ERR_INVALID_ARG),
+    (dict(k=257), sv.SPEC_ERR_INVALID_ARG),
+    (dict(nc=16, k=17), sv.SPEC_ERR_INVALID_ARG),
+    (dict(mc=8193), sv.SPEC_ERR_INVALID_ARG),
+    (dict(R=0), sv.SPEC_ERR_INVALID_ARG),
+    (dict(w=A8), sv.SPEC_ERR_ALIGNMENT),
+    (dict(ws=WS + 8), sv.SPEC_ERR_WORKSPACE),
+    (dict(wsb=1024), sv.SPEC_ERR_WORKSPACE),
+])
+def test_centroid_head_rejects_bad_arguments_on_host(lib, kw, code):
+    assert _head(lib, **kw) == code
+
+
+def _sparse(lib, **kw):
+    args = dict(t=A16, dt=sv.SPEC_BF16, ct=A16, cl=A16, cc=A16, stride=8192, tok=A16, temp=A16, ua=A16, ur=A16,
+                B=4, g=4, V=262144, out=A16, num=A16, dbg=None, ws=WS, wsb=1 << 30)
+    args.update(kw)
+    return lib.spec_verify_sample_sparse(args["t"], args["dt"], args["ct"], args["cl"], args["cc"], args["stride"],
+                                         args["tok"], args["temp"], args["ua"], args["ur"], args["B"], args["g"],
+                                         args["V"], args["out"], args["num"], args["dbg"], args["ws"], args["wsb"],
+                                         None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(t=None), sv.SPEC_ERR_INVALID_ARG),
+    (dict(ct=None), sv.SPEC_ERR_INVALID_ARG),
+    (dict(cc=None), sv.SPEC_ERR_INVALID_ARG),
+    (dict(stride=0), sv.SPEC_ERR_INVALID_ARG),
+    (dict(g=0), sv.SPEC_ERR_INVALID_ARG),
+    (dict(V=4100), sv.SPEC_ERR_INVALID_ARG),
+    (dict(dt=3), sv.SPEC_ERR_UNSUPPORTED),
+    (dict(t=A8), sv.SPEC_ERR_ALIGNMENT),
+    (dict(ws=WS + 8), sv.SPEC_ERR_WORKSPACE),
+    (dict(wsb=4096), sv.SPEC_ERR_WORKSPACE),
+])
+def test_sparse_rejects_bad_arguments_on_host(lib, kw, code):
+    assert _sparse(lib, **kw) == code
+
+
+def test_centroid_and_sparse_workspace_bytes(lib):
+    out = ctypes.c_size_t(0)
+    assert lib.spec_centroid_head_workspace_bytes(4, 2048, 32, ctypes.byref(out)) == sv.SPEC_OK
+    assert out.value >= 4 * 2048 * 4 + 4 * 32 * 4 + 4 * 33 * 4
+    assert lib.spec_centroid_head_workspace_bytes(4, 2048, 3000, ctypes.byref(out)) == sv.SPEC_ERR_INVALID_ARG
+    plain = sv.spec_verify_workspace_bytes(32, 4, 262144)
+    assert lib.spec_verify_sparse_workspace_bytes(32, 4, 262144, ctypes.byref(out)) == sv.SPEC_OK
+    assert out.value >= plain + 32 * 257 * 4     # per-chunk candidate offsets

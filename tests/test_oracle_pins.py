@@ -915,3 +915,18 @@ def test_mutation_sparse_fill_is_caught(monkeypatch):
                         lambda t, l, V: np.where(np.isin(np.arange(V), t), orig(t, l, V), 0.0))
     with pytest.raises(AssertionError):
         test_sparse_row_to_dense_gives_the_candidate_softmax()
+
+
+def test_verify_sample_sparse_empty_rows_accept_every_draft():
+    """No candidates: q = 0 everywhere, every draft is accepted (q(d) = 0) and
+    the bonus is the inverse CDF of p_gamma with the resample uniform."""
+    rng = np.random.default_rng(13)
+    V, gamma = 64, 3
+    target = rng.normal(0, 1.5, (1, gamma + 1, V))
+    empty = (np.zeros(0, np.int64), np.zeros(0))
+    res = oracle.verify_sample_sparse(target, [[empty] * gamma], np.array([[5, 9, 60]]), np.array([0.9]),
+                                      np.array([[0.999, 0.5, 0.0]]), np.array([0.37]))
+    r = res[0]
+    assert r.n == gamma and r.tokens[:gamma] == [5, 9, 60]
+    p = scipy.special.softmax(target[0, gamma] / 0.9)
+    assert r.tokens[gamma] == int(np.searchsorted(np.cumsum(p), 0.37, side="right"))
