@@ -422,6 +422,7 @@ def other_workloads(sv, dev, stream, args):
     res["topkp"] = topkp_workload(sv, dev, stream)
     res["multi"] = multi_workload(sv, dev, stream)
     res["lmhead"] = lmhead_workload(sv, dev, stream)
+    res["centroid"] = centroid_workload(sv, dev, stream)
     return res
 
 
@@ -572,6 +573,106 @@ def lmhead_workload(sv, dev, stream, steps=200):
     return res
 
 
+def centroid_workload(sv, dev, stream, steps=500):
+    """The centroid-masked draft head (V=262,144, H=1,536, 2,048 clusters, top
+    32) for R=4 draft rows (one sequence, gamma=4) and R=128 (32 sequences),
+    and the batched workload verified against sparse draft rows of 4,096
+    candidates (random tokens, logits = the target's + N(0, 0.3^2))."""
+    import torch
+
+    import workloads as wl
+    c = wl.CENTROID
+    m = wl.torch_centroid_model(dev)
+    V, H, Nc, K = m["V"], m["H"], m["n_clusters"], c["top_k"]
+    peak, _ = load_peaks()
+    res = {"V": V, "H": H, "n_clusters": Nc, "top_k": K}
+    g = torch.Generator(device=dev)
+    g.manual_seed(2024)
+    for R in (4, 128):
+        hids = [torch.randn(R, H, generator=g, device=dev).to(torch.bfloat16) for _ in range(4)]
+        ot = torch.empty((R, 8192), dtype=torch.int32, device=dev)
+        ol = torch.empty((R, 8192), dtype=torch.float32, device=dev)
+        oc = torch.empty((R,), dtype=torch.int32, device=dev)
+        ws = sv.make_centroid_head_workspace(R, Nc, K, device=dev)
+
+        def st(i, hids=hids, ot=ot, ol=ol, oc=oc, ws=ws):
+            sv.spec_centroid_head(hids[i % 4], m["centroids"], m["W_ord"], m["cluster_off"], m["ord2tok"], K,
+                                  ot, ol, oc, ws)
+        with torch.cuda.stream(stream):
+            st(0)
+        torch.cuda.synchronize()
+        cand = float(oc.float().mean().item())
+        loop = GraphLoop(st, steps, stream)
+        loop.run()
+        el = loop.run()
+        del loop
+        assert sv.spec_verify_status(ws, stream) == sv.SPEC_OK
+        nbytes = Nc * H * 2 + R * H * 2 + R * cand * (H * 2 + 16)  # centroids, hidden, gathered rows, outputs
+        us = el / steps * 1e6
+        res[f"head_R{R}"] = {"us_per_call": round(us, 2), "candidates_per_row": round(cand, 1),
+                             "bytes_per_call": int(nbytes), "gbs": round(nbytes / us / 1e3, 1),
+                             "frac_of_measured_hbm": round(nbytes / us / 1e3 / peak, 4), "steps": steps}
+    del m
+    torch.cuda.empty_cache()
+    # sparse verification of the batched workload
+    B, gam, v = 32, 4, 262144
+    pool = [wl.torch_round("batched", r, dev) for r in range(POOL)]
+    rounds = []
+    for p in pool:
+        rows = B * gam
+        keys = torch.rand(rows, v, generator=g, device=dev)
+        tok = torch.sort(torch.topk(keys, 4096, dim=1).indices, dim=1).values.to(torch.int32)
+        del keys
+        tgt = p["target"][:, :gam, :].reshape(rows, v).float()
+        lg = (torch.gather(tgt, 1, tok.long()) + 0.3 * torch.randn(rows, 4096, generator=g, device=dev)).contiguous()
+        del tgt
+        cnt = torch.full((rows,), 4096, dtype=torch.int32, device=dev)
+        T = p["temperature"].repeat_interleave(gam)[:, None]
+        u = torch.rand(rows, 4096, generator=g, device=dev).clamp_(min=1e-20)
+        pick = torch.argmax(lg / T - torch.log(-torch.log(u)), dim=1)
+        dtok = torch.gather(tok, 1, pick[:, None]).view(B, gam).contiguous()
+        rounds.append(dict(tok=tok, lg=lg, cnt=cnt, d=dtok))
+    wsv = sv.make_sparse_workspace(B, gam, v, device=dev)
+    o = torch.empty((B, gam + 1), dtype=torch.int32, device=dev)
+    n = torch.empty((B,), dtype=torch.int32, device=dev)
+
+    def sp(i):
+        p, q = pool[i % len(pool)], rounds[i % len(pool)]
+        sv.spec_verify_sample_sparse(p["target"], q["tok"], q["lg"], q["cnt"], q["d"], p["temperature"],
+                                     p["u_accept"], p["u_resample"], o, n, wsv)
+    with torch.cuda.stream(stream):
+        sp(0)
+    torch.cuda.synchronize()
+    loop = GraphLoop(sp, 1000, stream)
+    loop.run()
+    el = loop.run()
+    del loop
+    assert sv.spec_verify_status(wsv, stream) == sv.SPEC_OK
+    nb = B * (gam + 1) * v * 2 + B * gam * 4096 * 8
+    rps = 1000 / el
+    res["sparse_verify"] = {"rounds_per_s": round(rps, 1), "us_per_round": round(el / 1000 * 1e6, 2),
+                            "bytes_per_round": nb, "gbs": round(rps * nb / 1e9, 1),
+                            "frac_of_measured_hbm": round(rps * nb / 1e9 / peak, 4), "B": B, "gamma": gam, "V": v,
+                            "candidates_per_row": 4096, "logits_dtype": "bf16", "steps": 1000}
+    del pool, rounds
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_only_centroid(args):
+    import torch
+
+    import speculative_decoding_verification_54_gb300 as sv
+    from speculative_decoding_verification_54_gb300 import _build
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    _build.build()
+    sv.load()
+    stream = torch.cuda.Stream(device=dev)
+    res = centroid_workload(sv, dev, stream, steps=max(3, min(args.steps, 1000)))
+    print(json.dumps({"workload": "centroid", **res}), flush=True)
+
+
 def run_only_topkp(args):
     import torch
 
@@ -655,7 +756,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end host-buffer leg")
     ap.add_argument("--row-loads", choices=("ldg", "tma"), default=None,
                     help="row-reducer load path (default: the library's default, direct loads)")
-    ap.add_argument("--only", choices=("lmhead", "topkp"), default=None,
+    ap.add_argument("--only", choices=("lmhead", "topkp", "centroid"), default=None,
                     help="run one extra workload alone and print its figures (diagnostics, profiling)")
     args = ap.parse_args()
     if args.impl == "reference":
@@ -671,6 +772,8 @@ def main():
             run_only_lmhead(args)
         elif args.only == "topkp":
             run_only_topkp(args)
+        elif args.only == "centroid":
+            run_only_centroid(args)
         else:
             run_ours(args)
 

@@ -196,7 +196,7 @@ int spec_verify_sample_topkp(const void *target_logits, const void *draft_logits
  * the candidates (spec_verify_sample_sparse consumes exactly this layout).
  *
  * Layouts (device, row-major): hidden [R, H], centroids [n_clusters, H],
- * W_ord [V, H] bf16, 16-byte aligned, 256 <= H <= 4096, H % 256 == 0;
+ * W_ord [V, H] bf16, 16-byte aligned, 256 <= H <= 2048, H % 256 == 0;
  * cluster_off int32 [n_clusters+1] (non-decreasing, 0 .. V); ord2tok int32
  * [V] (a permutation of 0..V-1); out_tok int32 and out_logit f32
  * [R, max_cand]; out_count int32 [R].  1 <= n_clusters <= 8192,

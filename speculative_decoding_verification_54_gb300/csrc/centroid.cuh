@@ -12,13 +12,14 @@
 //   cluster_score_kernel   z[r, c] = h[r] . C[c]  (fp32 sums of bf16 products;
 //                          each warp holds one centroid, the CTA stages
 //                          kHeadRowBlock hidden rows in shared memory)
-//   cluster_topk_kernel    one CTA per row: bitonic sort of (score, -index)
-//                          keys; the top_k clusters (the lowest index first
-//                          among equal scores) and their candidate offsets
+//   cluster_topk_kernel    one CTA per row: radix select of the top_k scores
+//                          (the lowest index first among equal scores) and
+//                          the selected clusters' candidate offsets
 //   cand_logit_kernel      grid (top_k, R): one CTA per selected cluster, one
 //                          warp per token row, writes (token, logit) unsorted
-//   cand_sort_kernel       one CTA per row: sorts the candidates by token id
-//                          (the order the sparse verification searches in)
+//   cand_sort_kernel       one CTA per row: orders the candidates by token id
+//                          (the order the sparse verification searches in):
+//                          ranks from a bitmap of the row's tokens
 // The bulk of the bytes is the gathered embedding rows (top_k clusters of
 // about V / n_clusters rows of 2H bytes per hidden row): HBM/L2 bound.
 #pragma once
@@ -33,10 +34,11 @@ namespace specv {
 constexpr int kHeadThreads = 512;  // tk_sort_desc assumes 512-thread CTAs
 constexpr int kHeadWarps = kHeadThreads / 32;
 constexpr int kHeadRowBlock = 4;       // hidden rows staged per pass of cluster_score_kernel (32 KB)
-constexpr int kHeadMaxVecs = 16;       // 16-byte vectors per lane of one embedding row: H <= 4096
+constexpr int kHeadMaxVecs = 8;        // 16-byte vectors per lane of one embedding row: H <= 2048
 constexpr int kHeadMaxClusters = 8192;  // sorted in shared memory by cluster_topk_kernel
 constexpr int kHeadMaxTopK = 256;
 constexpr int kHeadMaxCand = 8192;     // candidates per row (sorted in shared memory)
+constexpr int kHeadBitmapV = 262144;   // vocabularies up to this size are ranked through a bitmap
 
 struct HeadParams {
   const __nv_bfloat16* hidden;     // [R, H]
@@ -115,35 +117,129 @@ __global__ void __launch_bounds__(kHeadThreads, 1) cluster_score_kernel(const __
   }
 }
 
+// Block-wide exclusive scan of one int per thread (all threads call); also
+// returns the block total.  s_w: kHeadWarps ints of shared memory.
+__device__ __forceinline__ int block_excl_scan(int v, int* s_w, int* total) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int incl = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += o;
+  }
+  if (lane == 31) s_w[warp] = incl;
+  __syncthreads();
+  int pre = 0, tot = 0;
+  for (int w = 0; w < kHeadWarps; ++w) {
+    const int x = s_w[w];
+    if (w < warp) pre += x;
+    tot += x;
+  }
+  __syncthreads();
+  *total = tot;
+  return pre + incl - v;
+}
+
 // ---- 2. top_k clusters of one row and their candidate offsets ----
+// A radix select (4 passes of 8-bit digits, most significant first) finds the
+// key of the top_k-th largest score; the clusters above it are kept, and of
+// those equal to it the lowest indices.  Thread t owns the clusters
+// [t*per, (t+1)*per), so the scans run in index order.  The selection is
+// written in index order (its order does not matter: the candidates are
+// sorted by token afterwards).
 __global__ void __launch_bounds__(kHeadThreads, 1) cluster_topk_kernel(const __grid_constant__ HeadParams p) {
-  extern __shared__ __align__(16) unsigned long long sk[];  // [n2] keys
+  extern __shared__ __align__(16) uint32_t keys[];  // [n_clusters]
+  __shared__ int hist[256];
+  __shared__ int s_w[kHeadWarps];
+  __shared__ uint32_t s_digit;
+  __shared__ int s_above;
   grid_dep_launch();
   grid_dep_wait();
-  const int r = blockIdx.x;
-  const int n2 = tk_pow2(p.n_clusters);
-  const float* z = p.scores + static_cast<size_t>(r) * p.n_clusters;
-  // key: the score's order-preserving bits, then the complemented index, so
-  // that a descending sort puts the lowest index first among equal scores
-  for (int c = threadIdx.x; c < n2; c += kHeadThreads)
-    sk[c] = (c < p.n_clusters)
-                ? (static_cast<unsigned long long>(logit_key(z[c])) << 32) | (0xffffffffu - static_cast<uint32_t>(c))
-                : 0ull;
-  __syncthreads();
-  tk_sort_desc(sk, n2);
-  int32_t* sel = p.sel + static_cast<size_t>(r) * p.top_k;
-  for (int k = threadIdx.x; k < p.top_k; k += kHeadThreads)
-    sel[k] = static_cast<int32_t>(0xffffffffu - static_cast<uint32_t>(sk[k] & 0xffffffffull));
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int32_t* pos = p.pos + static_cast<size_t>(r) * (p.top_k + 1);
-    int total = 0;
-    for (int k = 0; k < p.top_k; ++k) {
-      const int c = static_cast<int>(0xffffffffu - static_cast<uint32_t>(sk[k] & 0xffffffffull));
-      pos[k] = total;
-      // a padding key (possible only with NaN scores) decodes to c >= n_clusters: an empty cluster
-      if (c < p.n_clusters) total += max(0, min(p.cluster_off[c + 1], p.V) - max(p.cluster_off[c], 0));
+  const int r = blockIdx.x, t = threadIdx.x;
+  const int Nc = p.n_clusters;
+  const float* z = p.scores + static_cast<size_t>(r) * Nc;
+  for (int c = t; c < Nc; c += kHeadThreads) keys[c] = logit_key(z[c]);
+  uint32_t prefix = 0, mask = 0;
+  int remaining = p.top_k;  // how many of the keys matching the prefix still to take
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int i = t; i < 256; i += kHeadThreads) hist[i] = 0;
+    __syncthreads();
+    for (int c = t; c < Nc; c += kHeadThreads) {
+      const uint32_t k = keys[c];
+      if ((k & mask) == prefix) atomicAdd(&hist[(k >> shift) & 255u], 1);
     }
+    __syncthreads();
+    if (t < 32) {
+      // lane l owns digits 255-8l .. 248-8l (high to low); find the digit whose
+      // suffix count (keys with a larger digit) is below `remaining` and whose
+      // inclusive suffix count reaches it
+      int cnt[8], mine = 0;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        cnt[q] = hist[255 - 8 * t - q];
+        mine += cnt[q];
+      }
+      int incl = mine;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (t >= off) incl += o;
+      }
+      int run = incl - mine;  // keys with a digit above this lane's range
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        if (run < remaining && run + cnt[q] >= remaining) {
+          s_digit = static_cast<uint32_t>(255 - 8 * t - q);
+          s_above = run;
+        }
+        run += cnt[q];
+      }
+    }
+    __syncthreads();
+    prefix |= s_digit << shift;
+    mask |= 255u << shift;
+    remaining -= s_above;
+    __syncthreads();
+  }
+  // prefix: the top_k-th largest key; keep keys above it and the `remaining`
+  // lowest-index keys equal to it
+  const int per = (Nc + kHeadThreads - 1) / kHeadThreads;
+  const int c0 = min(Nc, t * per), c1 = min(Nc, c0 + per);
+  int eq = 0;
+  for (int c = c0; c < c1; ++c) eq += (keys[c] == prefix);
+  int tot;
+  int eq_before = block_excl_scan(eq, s_w, &tot);
+  int nsel = 0;
+  for (int c = c0; c < c1; ++c) {
+    const uint32_t k = keys[c];
+    nsel += (k > prefix) || (k == prefix && eq_before++ < remaining);
+  }
+  int sel_before = block_excl_scan(nsel, s_w, &tot);
+  // sizes of the selected clusters, in the same order, for the candidate offsets
+  int32_t* sel = p.sel + static_cast<size_t>(r) * p.top_k;
+  int32_t* pos = p.pos + static_cast<size_t>(r) * (p.top_k + 1);
+  eq_before = block_excl_scan(eq, s_w, &tot);
+  int size_sum = 0;
+  for (int c = c0; c < c1; ++c) {
+    const uint32_t k = keys[c];
+    if ((k > prefix) || (k == prefix && eq_before++ < remaining))
+      size_sum += max(0, min(p.cluster_off[c + 1], p.V) - max(p.cluster_off[c], 0));
+  }
+  int total;
+  int size_before = block_excl_scan(size_sum, s_w, &total);
+  eq_before = block_excl_scan(eq, s_w, &tot);
+  for (int c = c0; c < c1; ++c) {
+    const uint32_t k = keys[c];
+    if ((k > prefix) || (k == prefix && eq_before++ < remaining)) {
+      if (sel_before < p.top_k) {
+        sel[sel_before] = c;
+        pos[sel_before] = size_before;
+      }
+      ++sel_before;
+      size_before += max(0, min(p.cluster_off[c + 1], p.V) - max(p.cluster_off[c], 0));
+    }
+  }
+  if (t == 0) {
     pos[p.top_k] = total;
     if (total > p.max_cand) atomicOr(p.status, kStatusLimit);
     p.out_count[r] = min(total, p.max_cand);
@@ -168,38 +264,93 @@ __global__ void __launch_bounds__(kHeadThreads, 1) cand_logit_kernel(const __gri
   const int i0 = max(p.cluster_off[c], 0), i1 = min(p.cluster_off[c + 1], p.V);
   int32_t* otok = p.out_tok + static_cast<size_t>(r) * p.max_cand;
   float* olog = p.out_logit + static_cast<size_t>(r) * p.max_cand;
-  for (int i = i0 + warp; i < i1; i += kHeadWarps) {
+  // two embedding rows in flight per warp
+  for (int i = i0 + 2 * warp; i < i1; i += 2 * kHeadWarps) {
     const int slot = base + (i - i0);
     if (slot >= p.max_cand) break;  // overflow: reported by the selection kernel
-    uint4 e[kHeadMaxVecs];
-    load_row_vecs(p.W_ord + static_cast<size_t>(i) * p.H, nv, e);
-    const float lg = dot_row_smem(e, nv, reinterpret_cast<const uint4*>(hs));
+    const bool two = (i + 1 < i1) && (slot + 1 < p.max_cand);
+    uint4 e0[kHeadMaxVecs], e1[kHeadMaxVecs];
+    load_row_vecs(p.W_ord + static_cast<size_t>(i) * p.H, nv, e0);
+    if (two) load_row_vecs(p.W_ord + static_cast<size_t>(i + 1) * p.H, nv, e1);
+    const float l0 = dot_row_smem(e0, nv, reinterpret_cast<const uint4*>(hs));
+    const float l1 = two ? dot_row_smem(e1, nv, reinterpret_cast<const uint4*>(hs)) : 0.f;
     if (lane == 0) {
       otok[slot] = p.ord2tok[i];
-      olog[slot] = lg;
+      olog[slot] = l0;
+      if (two) {
+        otok[slot + 1] = p.ord2tok[i + 1];
+        olog[slot + 1] = l1;
+      }
     }
   }
 }
 
 // ---- 4. sort one row's candidates by token id (ascending) ----
+// Tokens are distinct ids in [0, V): for V <= kHeadBitmapV a candidate's rank
+// is the number of candidate tokens below it, read off a V-bit bitmap with a
+// prefix of its words' population counts (no comparison sort).  Larger
+// vocabularies use a bitonic sort of (token, logit) keys.
+constexpr size_t kHeadSortSmemBitmap = static_cast<size_t>(kHeadMaxCand) * 8 + (kHeadBitmapV / 32) * 8;
+
 __global__ void __launch_bounds__(kHeadThreads, 1) cand_sort_kernel(const __grid_constant__ HeadParams p) {
-  extern __shared__ __align__(16) unsigned long long sk[];
+  extern __shared__ __align__(16) unsigned long long dyn[];
+  __shared__ int s_w[kHeadWarps];
   grid_dep_launch();
   grid_dep_wait();
-  const int r = blockIdx.x;
+  const int r = blockIdx.x, t = threadIdx.x;
   const int n = p.out_count[r];
-  const int n2 = tk_pow2(max(n, 1));
   int32_t* otok = p.out_tok + static_cast<size_t>(r) * p.max_cand;
   float* olog = p.out_logit + static_cast<size_t>(r) * p.max_cand;
+  if (p.V <= kHeadBitmapV) {
+    int32_t* st_tok = reinterpret_cast<int32_t*>(dyn);
+    float* st_log = reinterpret_cast<float*>(st_tok + kHeadMaxCand);
+    uint32_t* bits = reinterpret_cast<uint32_t*>(st_log + kHeadMaxCand);
+    int* wpre = reinterpret_cast<int*>(bits + kHeadBitmapV / 32);
+    const int nw = (p.V + 31) / 32;
+    for (int i = t; i < nw; i += kHeadThreads) bits[i] = 0u;
+    for (int i = t; i < n; i += kHeadThreads) {
+      st_tok[i] = otok[i];
+      st_log[i] = olog[i];
+    }
+    __syncthreads();
+    for (int i = t; i < n; i += kHeadThreads) {
+      const int x = st_tok[i];
+      if (x >= 0 && x < p.V) atomicOr(&bits[x >> 5], 1u << (x & 31));
+    }
+    __syncthreads();
+    const int per = (nw + kHeadThreads - 1) / kHeadThreads;
+    const int w0 = min(nw, t * per), w1 = min(nw, w0 + per);
+    int cnt = 0;
+    for (int w = w0; w < w1; ++w) cnt += __popc(bits[w]);
+    int tot;
+    int run = block_excl_scan(cnt, s_w, &tot);
+    for (int w = w0; w < w1; ++w) {
+      wpre[w] = run;
+      run += __popc(bits[w]);
+    }
+    __syncthreads();
+    for (int i = t; i < n; i += kHeadThreads) {
+      const int x = st_tok[i];
+      if (x < 0 || x >= p.V) continue;  // not a token id: dropped
+      const int rank = wpre[x >> 5] + __popc(bits[x >> 5] & ((1u << (x & 31)) - 1u));
+      if (rank < n) {
+        otok[rank] = x;
+        olog[rank] = st_log[i];
+      }
+    }
+    return;
+  }
+  unsigned long long* sk = dyn;
+  const int n2 = tk_pow2(max(n, 1));
   // key: complemented token (descending sort = ascending tokens), then the
   // logit's bits; padding keys are 0 and sort last
-  for (int i = threadIdx.x; i < n2; i += kHeadThreads)
+  for (int i = t; i < n2; i += kHeadThreads)
     sk[i] = (i < n) ? (static_cast<unsigned long long>(0xffffffffu - static_cast<uint32_t>(otok[i])) << 32) |
                           __float_as_uint(olog[i])
                     : 0ull;
   __syncthreads();
   tk_sort_desc(sk, n2);
-  for (int i = threadIdx.x; i < n; i += kHeadThreads) {
+  for (int i = t; i < n; i += kHeadThreads) {
     otok[i] = static_cast<int32_t>(0xffffffffu - static_cast<uint32_t>(sk[i] >> 32));
     olog[i] = __uint_as_float(static_cast<uint32_t>(sk[i] & 0xffffffffull));
   }

@@ -71,12 +71,12 @@ int device_info(DeviceInfo* out) {
     if (cudaFuncSetAttribute(lmhead_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, d.lm_max_dyn) !=
         cudaSuccess)
       return SPEC_ERR_CUDA;
-    // the centroid head sorts up to kHeadMaxClusters / kHeadMaxCand keys of 8 B in shared memory
-    const int sort_smem = kHeadMaxCand * static_cast<int>(sizeof(unsigned long long));
-    if (cudaFuncSetAttribute(cluster_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, sort_smem) !=
-            cudaSuccess ||
-        cudaFuncSetAttribute(cand_sort_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, sort_smem) !=
-            cudaSuccess)
+    // the centroid head: cluster keys (4 B each) and the candidate ranking
+    // (candidates plus the token bitmap and its prefix) in shared memory
+    if (cudaFuncSetAttribute(cluster_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kHeadMaxClusters * 4) != cudaSuccess ||
+        cudaFuncSetAttribute(cand_sort_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kHeadSortSmemBitmap)) != cudaSuccess)
       return SPEC_ERR_CUDA;
     const char* env = std::getenv("SPECV_ROW_LOADS");
     d.path = (env != nullptr && std::strcmp(env, "tma") == 0) ? kTma : kLdg;
@@ -935,7 +935,7 @@ int spec_centroid_head(const void* hidden, const void* centroids, const void* W_
   if (hidden == nullptr || centroids == nullptr || W_ord == nullptr || cluster_off == nullptr ||
       ord2tok == nullptr || out_tok == nullptr || out_logit == nullptr || out_count == nullptr)
     return SPEC_ERR_INVALID_ARG;
-  if (R < 1 || R > 65535 || H < 256 || H > 32 * 8 * kHeadMaxVecs || (H % 256) != 0 || V < 1 ||
+  if (R < 1 || R > 65535 || H < 256 || H > 256 * kHeadMaxVecs || (H % 256) != 0 || V < 1 ||
       V > SPEC_MAX_VOCAB || n_clusters < 1 || n_clusters > kHeadMaxClusters || top_k < 1 || top_k > n_clusters ||
       top_k > kHeadMaxTopK || max_cand < 1 || max_cand > kHeadMaxCand)
     return SPEC_ERR_INVALID_ARG;
@@ -967,8 +967,9 @@ int spec_centroid_head(const void* hidden, const void* centroids, const void* W_
   hp.max_cand = max_cand;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const dim3 g1((n_clusters + kHeadWarps - 1) / kHeadWarps, (R + kHeadRowBlock - 1) / kHeadRowBlock);
-  const size_t sort1 = static_cast<size_t>(pow2_at_least(n_clusters)) * sizeof(unsigned long long);
-  const size_t sort2 = static_cast<size_t>(pow2_at_least(max_cand)) * sizeof(unsigned long long);
+  const size_t sort1 = static_cast<size_t>(n_clusters) * sizeof(uint32_t);
+  const size_t sort2 = (V <= kHeadBitmapV) ? kHeadSortSmemBitmap
+                                           : static_cast<size_t>(pow2_at_least(max_cand)) * sizeof(unsigned long long);
   if (launch_pdl(cluster_score_kernel, g1, dim3(kHeadThreads), 0, st, hp) != cudaSuccess ||
       launch_pdl(cluster_topk_kernel, dim3(R), dim3(kHeadThreads), sort1, st, hp) != cudaSuccess ||
       launch_pdl(cand_logit_kernel, dim3(top_k, R), dim3(kHeadThreads), 0, st, hp) != cudaSuccess ||

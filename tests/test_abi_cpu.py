@@ -250,7 +250,7 @@ def _head(lib, **kw):
     (dict(h=None), sv.SPEC_ERR_INVALID_ARG),
     (dict(off=None), sv.SPEC_ERR_INVALID_ARG),
     (dict(H=1000), sv.SPEC_ERR_INVALID_ARG),
-    (dict(H=8192), sv.SPEC_ERR_INVALID_ARG),
+    (dict(H=2304), sv.SPEC_ERR_INVALID_ARG),
     (dict(nc=0), sv.SPEC_ERR_INVALID_ARG),
     (dict(nc=8193), sv.SPEC_ERR_INVALID_ARG),
     (dict(k=0), sv.SPEC_ERR_INVALID_ARG),

@@ -36,7 +36,7 @@ import numpy as np
 __all__ = ["VerifyInputs", "LmheadInputs", "CONFIGS", "make_round",
            "make_lmhead_round", "make_lmhead_W", "make_custom", "make_multi", "f32_to_bf16_bits",
            "bf16_bits_to_f32", "torch_round", "torch_lmhead_round", "CENTROID", "CentroidModel",
-           "make_centroid_model", "make_centroid_round", "sample_sparse_drafts"]
+           "make_centroid_model", "make_centroid_round", "sample_sparse_drafts", "torch_centroid_model"]
 
 
 # ---------------------------------------------------------------------------
@@ -330,4 +330,4 @@ def torch_lmhead_round(r: int, device, W=None, seed: int = 0, B: int = 64,
 
 
 from .centroid import (CENTROID, CentroidModel, make_centroid_model,  # noqa: E402
-                       make_centroid_round, sample_sparse_drafts)
+                       make_centroid_round, sample_sparse_drafts, torch_centroid_model)

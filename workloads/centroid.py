@@ -124,3 +124,31 @@ def sample_sparse_drafts(cand, temperature, gamma: int, seed: int = 0, r: int = 
             else:
                 out[b, j] = tok[int(np.argmax(lg))]
     return out
+
+
+def torch_centroid_model(device, V: int | None = None, H: int | None = None, n_clusters: int | None = None,
+                         seed: int = 0) -> dict:
+    """The clustered-embedding recipe drawn with torch on ``device`` (a
+    different random stream from ``make_centroid_model``): W_ord [V, H] bf16,
+    centroids [n_clusters, H] bf16, cluster_off int32 [n_clusters+1], ord2tok
+    int32 [V]."""
+    import torch
+
+    c = CENTROID
+    V = c["V"] if V is None else V
+    H = c["H"] if H is None else H
+    n_clusters = c["n_clusters"] if n_clusters is None else n_clusters
+    g = torch.Generator(device=device)
+    g.manual_seed(seed * 7919 + 17)
+    cl = torch.randint(0, n_clusters, (V,), generator=g, device=device)
+    ord2tok = torch.argsort(cl.to(torch.int64) * V + torch.arange(V, device=device))
+    counts = torch.bincount(cl, minlength=n_clusters)
+    off = torch.zeros(n_clusters + 1, dtype=torch.int32, device=device)
+    off[1:] = torch.cumsum(counts, 0).to(torch.int32)
+    mu = c["mu_sd"] * torch.randn(n_clusters, H, generator=g, device=device)
+    cl_ord = cl[ord2tok]
+    w = (mu[cl_ord] + c["eps_sd"] * torch.randn(V, H, generator=g, device=device)).to(torch.bfloat16)
+    sums = torch.zeros(n_clusters, H, device=device).index_add_(0, cl_ord, w.float())
+    cen = torch.where(counts[:, None] > 0, sums / counts.clamp(min=1)[:, None], mu).to(torch.bfloat16)
+    return dict(V=V, H=H, n_clusters=n_clusters, W_ord=w.contiguous(), centroids=cen.contiguous(),
+                cluster_off=off, ord2tok=ord2tok.to(torch.int32).contiguous())
