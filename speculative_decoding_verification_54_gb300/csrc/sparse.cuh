@@ -87,16 +87,47 @@ __device__ __forceinline__ F2 warp_sum_f2(F2 v) {
   return v;
 }
 
-// Statistics of a sparse draft row, warp-wide: mk = fl(max logit * ks) and
-// log2 of sum 2^(fma(l, ks, -mk)) over the candidates (compensated sums).
-__device__ __forceinline__ RowStat cand_row_stats(const float* lg, int n, float ks) {
+// Partial statistics of a share [i0, i1) of a sparse draft row, warp-wide:
+// the raw maximum M and s = sum 2^(fma(l, ks, -fl(M*ks))) (compensated),
+// 32 entries per lane loaded at once.  Shares combine like the row
+// reducer's chunk partials.
+struct CandPartial {
+  float M, s;
+};
+
+__device__ __forceinline__ CandPartial cand_partial(const float* lg, int i0, int i1, float ks) {
   const int lane = threadIdx.x & 31;
-  float m = -FLT_MAX;
-  for (int i = lane; i < n; i += 32) m = fmaxf(m, __ldg(lg + i));
-  m = warp_max(m);
-  const float mk = m * ks;
-  float s = 0.f, c = 0.f;
-  for (int i = lane; i < n; i += 32) neumaier_add(s, c, ex2(fmaf(__ldg(lg + i), ks, -mk)));
+  constexpr int kBlk = 32;  // entries per lane per step
+  float M = -FLT_MAX, mk = kNegHuge, s = 0.f, c = 0.f;
+  for (int base = i0; base < i1; base += 32 * kBlk) {
+    float x[kBlk];
+#pragma unroll
+    for (int q = 0; q < kBlk; ++q) {
+      const int i = base + lane + 32 * q;
+      x[q] = (i < i1) ? __ldg(lg + i) : -INFINITY;
+    }
+    float m = M;
+#pragma unroll
+    for (int q = 0; q < kBlk; ++q) m = fmaxf(m, x[q]);
+    m = warp_max(m);
+    const float nmk = m * ks;
+    if (nmk != mk) {  // rescale what was summed so far (0 on the first step)
+      const float sc = ex2(mk - nmk);
+      s *= sc;
+      c *= sc;
+      mk = nmk;
+    }
+    M = m;
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+    for (int q = 0; q < kBlk; q += 4) {
+      a0 += ex2(fmaf(x[q], ks, -mk));
+      a1 += ex2(fmaf(x[q + 1], ks, -mk));
+      a2 += ex2(fmaf(x[q + 2], ks, -mk));
+      a3 += ex2(fmaf(x[q + 3], ks, -mk));
+    }
+    neumaier_add(s, c, (a0 + a1) + (a2 + a3));
+  }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) {
     const float os = __shfl_xor_sync(0xffffffffu, s, off);
@@ -104,21 +135,20 @@ __device__ __forceinline__ RowStat cand_row_stats(const float* lg, int n, float 
     neumaier_add(s, c, os);
     c += oc;
   }
-  RowStat st;
-  st.mk = (n > 0) ? mk : kNegHuge;
-  st.argmax = -1;
-  st.pad = 0;
-  st.lse2 = log2f(s + c);
-  return st;
+  return CandPartial{M, s + c};
 }
 
 // Normalised weights of the residual row pair: p_n(x) from a target logit,
 // q_n(x) from a candidate's logit (explicitly rounded operations: every
 // evaluation of the same entry gives the same bits).
+// Both in units of 2^mkp * S_p (the target row's scaled maximum and sum), so
+// p costs one exp2: p(x) = 2^(fma(x, ks, -mkp)), q(x) = 2^(fma(l, ks, -mkq))
+// * qs with qs = S_p / S_q.  Chunk masses in these units are proportional to
+// the true ones, which is all the inverse CDF needs.
 struct SparseW {
-  float ks, mkp, invSp, mkq, invSq;
-  __device__ __forceinline__ float p(float xp) const { return __fmul_rn(ex2(fmaf(xp, ks, -mkp)), invSp); }
-  __device__ __forceinline__ float q(float lq) const { return __fmul_rn(ex2(fmaf(lq, ks, -mkq)), invSq); }
+  float ks, mkp, mkq, qs;
+  __device__ __forceinline__ float p(float xp) const { return ex2(fmaf(xp, ks, -mkp)); }
+  __device__ __forceinline__ float q(float lq) const { return __fmul_rn(ex2(fmaf(lq, ks, -mkq)), qs); }
 };
 
 // Candidates of draft row `row` (the caller's count, clamped to [0, stride]).
@@ -204,6 +234,7 @@ __global__ void __launch_bounds__(kSparseThreads, 1) sparse_tail_kernel(const __
   __shared__ RowStat rs[2 * 31 + 1];
   __shared__ SeqState s_seq;
   __shared__ float s_xq[32];
+  __shared__ CandPartial s_cp[31 * kSparseWarps];
   __shared__ int s_lo, s_hi, s_last;
   __shared__ int32_t st_tok[kSparseStage];
   __shared__ float st_q[kSparseStage];
@@ -227,9 +258,19 @@ __global__ void __launch_bounds__(kSparseThreads, 1) sparse_tail_kernel(const __
         din.u = p.dp.u_accept[b * g + lane];
       }
     }
-  } else if (!greedy) {
-    // the drafts' own logits: a search of each candidate list (-inf if absent)
-    for (int j = warp - 1; j < g; j += kSparseWarps - 1) {
+  }
+  const float u_res = greedy ? 0.f : p.u_resample[b];
+  grid_dep_wait();
+
+  // ---- target rows from the partials (warps 0..gamma); meanwhile the other
+  // warps look the drafts up in their candidate lists (-inf if absent) ----
+  for (int r = warp; r <= g; r += kSparseWarps) {
+    const RowStat st = combine_row<4>(p.partials + static_cast<size_t>(b * slots + r) * p.cpr, p.cpr, !greedy);
+    if (lane == 0) rs[r] = st;
+  }
+  if (!greedy) {
+    const int w0 = (g + 1 < kSparseWarps) ? g + 1 : 0;  // with gamma >= 15 every warp takes a share
+    for (int j = warp - w0; warp >= w0 && j < g; j += kSparseWarps - w0) {
       const int row = b * g + j;
       const int d = p.dp.draft_tokens[row];
       const int n = cand_n(p, row);
@@ -239,19 +280,35 @@ __global__ void __launch_bounds__(kSparseThreads, 1) sparse_tail_kernel(const __
       if (lane == 0) s_xq[j] = hit ? __ldg(p.cand_logit + static_cast<size_t>(row) * p.stride + i) : -INFINITY;
     }
   }
-  const float u_res = greedy ? 0.f : p.u_resample[b];
-  grid_dep_wait();
-
-  // ---- target rows from the partials, draft rows from their candidates ----
-  for (int r = warp; r < (greedy ? g + 1 : slots); r += kSparseWarps) {
-    RowStat st;
-    if (r <= g) {
-      st = combine_row<4>(p.partials + static_cast<size_t>(b * slots + r) * p.cpr, p.cpr, !greedy);
-    } else {
-      const int row = b * g + (r - g - 1);
-      st = cand_row_stats(p.cand_logit + static_cast<size_t>(row) * p.stride, cand_n(p, row), ks);
+  // ---- draft rows from their candidates: each row split over wpr warps ----
+  if (!greedy) {
+    const int wpr = max(1, kSparseWarps / g);
+    for (int jj = warp / wpr; jj < g && warp < wpr * g; jj += kSparseWarps / wpr) {
+      const int row = b * g + jj, k = warp % wpr;
+      const int n = cand_n(p, row);
+      const CandPartial cp =
+          cand_partial(p.cand_logit + static_cast<size_t>(row) * p.stride, n * k / wpr, n * (k + 1) / wpr, ks);
+      if (lane == 0) s_cp[jj * kSparseWarps + k] = cp;
     }
-    if (lane == 0) rs[r] = st;
+  }
+  __syncthreads();
+  if (!greedy && threadIdx.x < g) {
+    // fold the shares of draft row jj: rescale each to the row's scaled maximum
+    const int jj = threadIdx.x, wpr = max(1, kSparseWarps / g);
+    float M = -FLT_MAX;
+    for (int k = 0; k < wpr; ++k) M = fmaxf(M, s_cp[jj * kSparseWarps + k].M);
+    const float mk = M * ks;
+    float sum = 0.f, c = 0.f;
+    for (int k = 0; k < wpr; ++k) {
+      const CandPartial cp = s_cp[jj * kSparseWarps + k];
+      if (cp.s > 0.f) neumaier_add(sum, c, cp.s * ex2(cp.M * ks - mk));
+    }
+    RowStat st;
+    st.mk = (cand_n(p, b * g + jj) > 0) ? mk : kNegHuge;
+    st.argmax = -1;
+    st.pad = 0;
+    st.lse2 = log2f(sum + c);
+    rs[g + 1 + jj] = st;
   }
   __syncthreads();
   if (warp == 0) {
@@ -279,9 +336,8 @@ __global__ void __launch_bounds__(kSparseThreads, 1) sparse_tail_kernel(const __
   SparseW f;
   f.ks = s.ks;
   f.mkp = rs[s.n].mk;
-  f.invSp = ex2(-rs[s.n].lse2);
   f.mkq = rs[g + 1 + s.n].mk;
-  f.invSq = ex2(-rs[g + 1 + s.n].lse2);
+  f.qs = ex2(rs[s.n].lse2 - rs[g + 1 + s.n].lse2);
   const size_t rowp_n = static_cast<size_t>(b) * (g + 1) + s.n;
 
   if (s.mode == kModeResidual) {
@@ -324,23 +380,29 @@ __global__ void __launch_bounds__(kSparseThreads, 1) sparse_tail_kernel(const __
         const int k = lane + 32 * j;
         v[j] = (k < nvec) ? __ldg(vp + k) : neg_inf_vec<T>();
       }
-      F2 sp = f2_from(0.f);
+      // compensated (Neumaier) sums per lane, four independent chains;
+      // lanes combine in two-float
+      float sa[4] = {0.f, 0.f, 0.f, 0.f}, ca[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int j = 0; j < kVecPerLane; ++j) {
         float xp[P];
         Elt<T>::unpack(v[j], xp);
 #pragma unroll
-        for (int k = 0; k < P; ++k) sp = f2_add(sp, f2_from(f.p(xp[k])));
+        for (int k = 0; k < P; ++k) neumaier_add(sa[k & 3], ca[k & 3], f.p(xp[k]));
       }
+      F2 sp = f2_from(0.f);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) sp = f2_add(sp, f2_add(f2_from(sa[k]), f2_from(ca[k])));
       // minus min(p_n, q_n) over the chunk's candidates
-      F2 sm = f2_from(0.f);
+      float s1 = 0.f, c1m = 0.f;
       for (int i = a + lane; i < e; i += 32) {
         const int x = staged ? st_tok[i] : __ldg(tok + lo + i);
         if (x < 0 || x >= p.V) continue;  // not a token: no weight to take off
         const float q = staged ? st_q[i] : f.q(__ldg(lg + lo + i));
         const float pp = f.p(load_logit<T>(p.target, rowp_n * p.V + x));
-        sm = f2_add(sm, f2_from(fminf(pp, q)));
+        neumaier_add(s1, c1m, fminf(pp, q));
       }
+      F2 sm = f2_add(f2_from(s1), f2_from(c1m));
       sp = warp_sum_f2(sp);
       sm = warp_sum_f2(sm);
       const F2 d = f2_sub(sp, sm);

@@ -652,7 +652,8 @@ int run_sparse(const Common& a, const SparseArgs& c) {
   dp.status = status;
   dp.gamma = a.gamma;
   dp.V = a.V;
-  // one tail CTA per SM over the batch (at most 16 per sequence)
+  // one tail CTA per SM over the batch (at most 16 per sequence); two per SM
+  // (64 registers, 9 parts for B=32) measured the same
   int parts = dev.sms / a.B;
   if (parts > 16) parts = 16;
   if (parts > pl.cpr) parts = pl.cpr;
