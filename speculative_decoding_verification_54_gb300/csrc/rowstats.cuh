@@ -64,6 +64,8 @@ struct RowStatsParams {
   int* status;
   int B, gamma, V, CE, cpr;
   int draft_only;  // skip the target rows (their statistics come from the lm_head epilogue)
+  float* submax;   // nullptr, or [slots*cpr*kVecPerLane]: the maxima of each chunk's kVecPerLane
+                   // blocks of 32 vectors (the top-k / top-p collection bound)
   int debug;       // bit 0: forced-timeout self-test
 };
 
@@ -257,6 +259,35 @@ __device__ __forceinline__ void finish_item(const RowStatsParams& p, const Item&
   const float4 r = (d.mode == kRowFull) ? reduce_full<T>(v, d.ks)
                                         : reduce_argmax<T>(v, d.chunk * p.CE, lane);
   if (lane == 0) p.partials[static_cast<size_t>(d.slot) * p.cpr + d.chunk] = r;
+  if (p.submax != nullptr) {
+    // block j of the chunk is vector slot j of every lane (32 consecutive
+    // vectors).  A warp reduce-scatter: each exchange halves the values a
+    // lane holds, so the 8 maxima take 4 + 2 + 1 + 1 + 1 shuffles; lane l
+    // ends with block ((l >> 4) & 1) * 4 + ((l >> 3) & 1) * 2 + ((l >> 2) & 1).
+    static_assert(kVecPerLane == 8, "the reduce-scatter below is written for 8 blocks");
+    float m8[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) m8[j] = vec_max<T>(v[j]);
+    const bool h16 = lane & 16, h8 = lane & 8, h4 = lane & 4;
+    float m4[4], m2[2];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float keep = h16 ? m8[q + 4] : m8[q], give = h16 ? m8[q] : m8[q + 4];
+      m4[q] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, give, 16));
+    }
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const float keep = h8 ? m4[q + 2] : m4[q], give = h8 ? m4[q] : m4[q + 2];
+      m2[q] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, give, 8));
+    }
+    float m = fmaxf(h4 ? m2[1] : m2[0], __shfl_xor_sync(0xffffffffu, h4 ? m2[0] : m2[1], 4));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+    if ((lane & 3) == 0) {
+      const int j = (h16 ? 4 : 0) + (h8 ? 2 : 0) + (h4 ? 1 : 0);
+      p.submax[(static_cast<size_t>(d.slot) * p.cpr + d.chunk) * kVecPerLane + j] = m;
+    }
+  }
 }
 
 template <typename T, int kPath>

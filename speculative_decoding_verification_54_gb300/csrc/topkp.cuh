@@ -51,7 +51,12 @@ struct TopkParams {
   float2* rowd;              // [B*(2*gamma+1)] {logit of the row's draft token, 1 if kept else 0}
   const int32_t* draft_tokens;  // [B, gamma]
   int* status;
-  int B, gamma, V, top_k;
+  // the row reducer's chunk partials and the lists topk_collect_kernel fills
+  // from them (nullptr: the select kernel finds K on its own)
+  const float* submax;           // [B*(2*gamma+1)*cpr*kVecPerLane] maxima of 32-vector blocks
+  unsigned long long* pre_keys;  // [B*(2*gamma+1)][kTkStore] (key << 32 | ~index)
+  int* pre_count;                // [B*(2*gamma+1)]; reset to 0 by the select kernel
+  int B, gamma, V, top_k, cpr, CE;
   float top_p;
 };
 
@@ -288,6 +293,158 @@ __device__ __forceinline__ int tk_pow2(int n) {
   return p2;
 }
 
+// Block-wide radix select over n keys in shared memory (4 passes of 8-bit
+// digits, most significant first): the k-th largest key (1 <= k <= n).
+// *greater receives how many keys are strictly larger.  All threads call;
+// every thread returns the same.
+__device__ __forceinline__ uint32_t tk_block_kth(const uint32_t* keys, int n, int k, int* hist, int* s_val,
+                                                 int* greater) {
+  const int t = threadIdx.x;
+  uint32_t prefix = 0, mask = 0;
+  int remaining = k;
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int i = t; i < 256; i += blockDim.x) hist[i] = 0;
+    __syncthreads();
+    for (int c = t; c < n; c += blockDim.x) {
+      const uint32_t key = keys[c];
+      if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1);
+    }
+    __syncthreads();
+    if (t < 32) {
+      // lane l owns digits 255-8l .. 248-8l; the digit reached by `remaining`
+      int cnt[8], mine = 0;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        cnt[q] = hist[255 - 8 * t - q];
+        mine += cnt[q];
+      }
+      int incl = mine;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (t >= off) incl += o;
+      }
+      int run = incl - mine;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        if (run < remaining && run + cnt[q] >= remaining) {
+          s_val[0] = 255 - 8 * t - q;
+          s_val[1] = run;
+        }
+        run += cnt[q];
+      }
+    }
+    __syncthreads();
+    prefix |= static_cast<uint32_t>(s_val[0]) << shift;
+    mask |= 255u << shift;
+    remaining -= s_val[1];
+    __syncthreads();
+  }
+  *greater = k - remaining;
+  return prefix;
+}
+
+constexpr int kTkCollectMaxBlocks = 4096;  // block maxima held in shared memory
+
+// GPU-wide collection of K's superset, grid (rows, parts).  The row reducer
+// records the maximum of every block of 32 vectors (256 bf16 or 128 fp32
+// logits); those maxima are logits themselves, so the k-th largest of them,
+// M_k, is a lower bound on the k-th largest logit: K lies inside the blocks
+// whose maximum reaches M_k.  The row's CTAs deal those blocks to their warps
+// (one vector per lane) and append the logits >= M_k to the row's list with
+// warp-aggregated atomics (the select kernel sorts, so the order does not
+// matter).  Rows with more than kTkCollectMaxBlocks blocks are left to the
+// select kernel.
+template <typename T>
+__global__ void __launch_bounds__(kTkThreads, 2) topk_collect_kernel(const __grid_constant__ TopkParams p) {
+  constexpr int P = Elt<T>::kPerVec;
+  __shared__ uint32_t ck[kTkCollectMaxBlocks];
+  __shared__ uint16_t qlist[kTkCollectMaxBlocks];  // the qualifying blocks, in order
+  __shared__ int hist[256];
+  __shared__ int s_val[2];
+  __shared__ int s_w[kTkWarps];
+  grid_dep_launch();
+  grid_dep_wait();
+  const int g = p.gamma, slots = 2 * g + 1;
+  const int slot = blockIdx.x, b = slot / slots, t = slot - b * slots;
+  const bool greedy = seq_is_greedy(p.temperature, b);
+  const int nb = p.cpr * kVecPerLane;
+  if ((t > g && greedy) || nb > kTkCollectMaxBlocks) return;
+  const int k = greedy ? 1 : min(p.top_k, p.V);
+  const float* sm = p.submax + static_cast<size_t>(slot) * nb;
+  for (int c = threadIdx.x; c < nb; c += kTkThreads) ck[c] = logit_key(__ldcg(sm + c));
+  __syncthreads();
+  int greater;  // unused: the list keeps every logit >= the bound
+  const uint32_t thr = (k < nb) ? tk_block_kth(ck, nb, k, hist, s_val, &greater) : 0u;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint8_t* row = (t <= g) ? static_cast<const uint8_t*>(p.target) +
+                                      (static_cast<size_t>(b) * (g + 1) + t) * p.V * sizeof(T)
+                                : static_cast<const uint8_t*>(p.draft) +
+                                      (static_cast<size_t>(b) * g + (t - g - 1)) * p.V * sizeof(T);
+  unsigned long long* out = p.pre_keys + static_cast<size_t>(slot) * kTkStore;
+  int* cnt = p.pre_count + slot;
+  const int nvec_row = p.V / P;
+  // the qualifying blocks, compacted in order: thread t checks blocks
+  // [t*per, (t+1)*per), a block scan gives each its position
+  const int per = (nb + kTkThreads - 1) / kTkThreads;
+  const int q0 = min(nb, static_cast<int>(threadIdx.x) * per), q1 = min(nb, q0 + per);
+  int mine = 0;
+  for (int q = q0; q < q1; ++q) mine += (ck[q] >= thr);
+  int incl = mine;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += o;
+  }
+  if (lane == 31) s_w[warp] = incl;
+  __syncthreads();
+  int before = incl - mine, nq = 0;
+  for (int w = 0; w < kTkWarps; ++w) {
+    if (w < warp) before += s_w[w];
+    nq += s_w[w];
+  }
+  for (int q = q0; q < q1; ++q)
+    if (ck[q] >= thr) qlist[before++] = static_cast<uint16_t>(q);
+  __syncthreads();
+  // block q of chunk c covers the row's vectors c*CE/P + 32j .. +31 (q = 8c + j)
+  const int stride = gridDim.y * kTkWarps;
+  for (int qi = blockIdx.y * kTkWarps + warp; qi < nq; qi += stride) {
+    const int q = qlist[qi];
+    const int c = q / kVecPerLane, j = q - c * kVecPerLane;
+    const int vi = c * (p.CE / P) + 32 * j + lane;  // this lane's vector of the row
+    const bool in = (32 * j + lane) < (p.CE / P) && vi < nvec_row;
+    const uint4 u = in ? __ldg(reinterpret_cast<const uint4*>(row) + vi) : neg_inf_vec<T>();
+    float x[P];
+    Elt<T>::unpack(u, x);
+    uint32_t hits = 0;
+#pragma unroll
+    for (int e = 0; e < P; ++e)
+      if (in && logit_key(x[e]) >= thr) hits |= 1u << e;
+    const int nh = __popc(hits);
+    int incl = nh;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += o;
+    }
+    const int total = __shfl_sync(0xffffffffu, incl, 31);
+    if (total == 0) continue;
+    int base = 0;
+    if (lane == 31) base = atomicAdd(cnt, total);
+    base = __shfl_sync(0xffffffffu, base, 31) + incl - nh;
+#pragma unroll
+    for (int e = 0; e < P; ++e) {
+      if ((hits >> e) & 1u) {
+        if (base < kTkStore) {
+          const uint32_t idx = static_cast<uint32_t>(vi * P + e);
+          out[base] = (static_cast<unsigned long long>(logit_key(x[e])) << 32) | (0xffffffffu - idx);
+        }
+        ++base;
+      }
+    }
+  }
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kTkThreads, 2) topk_select_kernel(const __grid_constant__ TopkParams p) {
   constexpr int P = Elt<T>::kPerVec;
@@ -296,6 +453,7 @@ __global__ void __launch_bounds__(kTkThreads, 2) topk_select_kernel(const __grid
   __shared__ F2 s_wtot[kTkWarps];
   __shared__ int s_digit, s_remaining, s_count, s_cut;
   grid_dep_launch();
+  grid_dep_wait();  // the collection kernel's lists
   const int g = p.gamma, slots = 2 * g + 1;
   const int slot = blockIdx.x, b = slot / slots, t = slot - b * slots;
   const bool greedy = seq_is_greedy(p.temperature, b);
@@ -315,7 +473,17 @@ __global__ void __launch_bounds__(kTkThreads, 2) topk_select_kernel(const __grid
   const int srank = k / 8 + 8;
   uint32_t prefix = 0, pmask = 0;
   int count = -1;
-  if (p.V >= 4096 && srank <= smp.count()) {
+  if (p.pre_count != nullptr) {  // the list topk_collect_kernel gathered, if it is complete
+    const int pc = __ldcg(p.pre_count + slot);
+    if (pc >= k && pc <= kTkStore) {
+      const unsigned long long* pk = p.pre_keys + static_cast<size_t>(slot) * kTkStore;
+      for (int i = threadIdx.x; i < pc; i += kTkThreads) sk[i] = __ldcg(pk + i);
+      count = pc;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) p.pre_count[slot] = 0;  // ready for the next call
+  }
+  if (count < 0 && p.V >= 4096 && srank <= smp.count()) {
     tk_radix_select<T>(row, smp, srank, hist, &s_digit, &s_remaining, &prefix, &pmask);
     count = tk_collect<T>(row, p.V, prefix, pmask, sk, &s_count);
     if (count < k || count > kTkStore) count = -1;
