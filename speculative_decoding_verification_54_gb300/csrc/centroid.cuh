@@ -35,7 +35,7 @@ constexpr int kHeadThreads = 512;  // tk_sort_desc assumes 512-thread CTAs
 constexpr int kHeadWarps = kHeadThreads / 32;
 constexpr int kHeadRowBlock = 4;       // hidden rows staged per pass of cluster_score_kernel (32 KB)
 constexpr int kHeadMaxVecs = 8;        // 16-byte vectors per lane of one embedding row: H <= 2048
-constexpr int kHeadMaxClusters = 8192;  // sorted in shared memory by cluster_topk_kernel
+constexpr int kHeadMaxClusters = 8192;  // cluster keys held in shared memory by cluster_topk_kernel
 constexpr int kHeadMaxTopK = 256;
 constexpr int kHeadMaxCand = 8192;     // candidates per row (sorted in shared memory)
 constexpr int kHeadBitmapV = 262144;   // vocabularies up to this size are ranked through a bitmap
@@ -141,9 +141,9 @@ __device__ __forceinline__ int block_excl_scan(int v, int* s_w, int* total) {
 }
 
 // ---- 2. top_k clusters of one row and their candidate offsets ----
-// A radix select (4 passes of 8-bit digits, most significant first) finds the
-// key of the top_k-th largest score; the clusters above it are kept, and of
-// those equal to it the lowest indices.  Thread t owns the clusters
+// A radix select (tk_block_kth: 4 passes of 8-bit digits) finds the key of
+// the top_k-th largest score; the clusters above it are kept, and of those
+// equal to it the lowest indices.  Thread t owns the clusters
 // [t*per, (t+1)*per), so the scans run in index order.  The selection is
 // written in index order (its order does not matter: the candidates are
 // sorted by token afterwards).
@@ -151,56 +151,17 @@ __global__ void __launch_bounds__(kHeadThreads, 1) cluster_topk_kernel(const __g
   extern __shared__ __align__(16) uint32_t keys[];  // [n_clusters]
   __shared__ int hist[256];
   __shared__ int s_w[kHeadWarps];
-  __shared__ uint32_t s_digit;
-  __shared__ int s_above;
+  __shared__ int s_val[2];
   grid_dep_launch();
   grid_dep_wait();
   const int r = blockIdx.x, t = threadIdx.x;
   const int Nc = p.n_clusters;
   const float* z = p.scores + static_cast<size_t>(r) * Nc;
   for (int c = t; c < Nc; c += kHeadThreads) keys[c] = logit_key(z[c]);
-  uint32_t prefix = 0, mask = 0;
-  int remaining = p.top_k;  // how many of the keys matching the prefix still to take
-  for (int shift = 24; shift >= 0; shift -= 8) {
-    for (int i = t; i < 256; i += kHeadThreads) hist[i] = 0;
-    __syncthreads();
-    for (int c = t; c < Nc; c += kHeadThreads) {
-      const uint32_t k = keys[c];
-      if ((k & mask) == prefix) atomicAdd(&hist[(k >> shift) & 255u], 1);
-    }
-    __syncthreads();
-    if (t < 32) {
-      // lane l owns digits 255-8l .. 248-8l (high to low); find the digit whose
-      // suffix count (keys with a larger digit) is below `remaining` and whose
-      // inclusive suffix count reaches it
-      int cnt[8], mine = 0;
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        cnt[q] = hist[255 - 8 * t - q];
-        mine += cnt[q];
-      }
-      int incl = mine;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int o = __shfl_up_sync(0xffffffffu, incl, off);
-        if (t >= off) incl += o;
-      }
-      int run = incl - mine;  // keys with a digit above this lane's range
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        if (run < remaining && run + cnt[q] >= remaining) {
-          s_digit = static_cast<uint32_t>(255 - 8 * t - q);
-          s_above = run;
-        }
-        run += cnt[q];
-      }
-    }
-    __syncthreads();
-    prefix |= s_digit << shift;
-    mask |= 255u << shift;
-    remaining -= s_above;
-    __syncthreads();
-  }
+  __syncthreads();
+  int greater;
+  const uint32_t prefix = tk_block_kth(keys, Nc, p.top_k, hist, s_val, &greater);
+  const int remaining = p.top_k - greater;  // keys equal to the k-th to take, lowest index first
   // prefix: the top_k-th largest key; keep keys above it and the `remaining`
   // lowest-index keys equal to it
   const int per = (Nc + kHeadThreads - 1) / kHeadThreads;

@@ -64,7 +64,7 @@ struct RowStatsParams {
   int* status;
   int B, gamma, V, CE, cpr;
   int draft_only;  // skip the target rows (their statistics come from the lm_head epilogue)
-  float* submax;   // nullptr, or [slots*cpr*kVecPerLane]: the maxima of each chunk's kVecPerLane
+  float* submax;   // [slots*cpr*kVecPerLane] with kSubMax: the maxima of each chunk's kVecPerLane
                    // blocks of 32 vectors (the top-k / top-p collection bound)
   int debug;       // bit 0: forced-timeout self-test
 };
@@ -253,13 +253,13 @@ __device__ __forceinline__ bool next_live(const RowStatsParams& p, ItemIter& it,
   return false;
 }
 
-template <typename T>
+template <typename T, bool kSubMax>
 __device__ __forceinline__ void finish_item(const RowStatsParams& p, const Item& d,
                                             const uint4 (&v)[kVecPerLane], int lane) {
   const float4 r = (d.mode == kRowFull) ? reduce_full<T>(v, d.ks)
                                         : reduce_argmax<T>(v, d.chunk * p.CE, lane);
   if (lane == 0) p.partials[static_cast<size_t>(d.slot) * p.cpr + d.chunk] = r;
-  if (p.submax != nullptr) {
+  if constexpr (kSubMax) {
     // block j of the chunk is vector slot j of every lane (32 consecutive
     // vectors).  A warp reduce-scatter: each exchange halves the values a
     // lane holds, so the 8 maxima take 4 + 2 + 1 + 1 + 1 shuffles; lane l
@@ -290,7 +290,7 @@ __device__ __forceinline__ void finish_item(const RowStatsParams& p, const Item&
   }
 }
 
-template <typename T, int kPath>
+template <typename T, int kPath, bool kSubMax = false>
 __global__ void __launch_bounds__(kRowThreads, (kPath == kLdg) ? 2 : 1)
     rowstats_kernel(const RowStatsParams p) {
   extern __shared__ __align__(128) uint8_t ring[];  // kTma only
@@ -323,7 +323,7 @@ __global__ void __launch_bounds__(kRowThreads, (kPath == kLdg) ? 2 : 1)
         const int k = lane + 32 * j;
         v[j] = (k < d.nvec) ? ld_stream(d.src + k) : neg_inf_vec<T>();
       }
-      finish_item<T>(p, d, v, lane);
+      finish_item<T, kSubMax>(p, d, v, lane);
     }
   } else {
     // private ring of kTmaStages chunks per warp; lane 0 issues the copies
@@ -371,7 +371,7 @@ __global__ void __launch_bounds__(kRowThreads, (kPath == kLdg) ? 2 : 1)
         }
         ++issued;
       }
-      finish_item<T>(p, d, v, lane);
+      finish_item<T, kSubMax>(p, d, v, lane);
     }
     if (!ok) {  // drain: copies still in flight land before the CTA exits
       for (int k = consumed; k < issued; ++k)

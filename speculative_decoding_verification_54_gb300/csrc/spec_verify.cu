@@ -325,7 +325,7 @@ int run_topkp(const Common& a, int top_k, float top_p) {
   rp.CE = pl.CE;
   rp.cpr = pl.cpr;
   rp.submax = reinterpret_cast<float*>(ws + L.submax);
-  if (launch_pdl(rowstats_kernel<T, kLdg>, dim3(pl.grid), dim3(kRowThreads), 0, a.stream, rp) != cudaSuccess)
+  if (launch_pdl(rowstats_kernel<T, kLdg, true>, dim3(pl.grid), dim3(kRowThreads), 0, a.stream, rp) != cudaSuccess)
     return SPEC_ERR_CUDA;
   // 2. the logits at or above each row's k-th largest block maximum
   k.submax = rp.submax;
