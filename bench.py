@@ -329,6 +329,7 @@ def e2e_leg(sv, pool, out, num, wsp, dev, stream, args, ws_n):
         hout.copy_(out, non_blocking=True)
         hnum.copy_(num, non_blocking=True)
 
+    torch.cuda.synchronize()  # inputs built on the default stream are complete
     with torch.cuda.stream(stream):
         for i in range(3):
             e2e_step(i)
@@ -405,6 +406,7 @@ def other_workloads(sv, dev, stream, args):
             p = pool[i % len(pool)]
             sv.spec_verify_sample(p["target"], p["draft"], p["draft_tokens"], p["temperature"],
                                   p["u_accept"], p["u_resample"], o, n, w)
+        torch.cuda.synchronize()  # inputs built on the default stream are complete
         with torch.cuda.stream(stream):
             st(0)
         torch.cuda.synchronize()
@@ -443,6 +445,7 @@ def topkp_workload(sv, dev, stream, steps=1000, top_k=64, top_p=0.95):
         sv.spec_verify_sample_topkp(p["target"], p["draft"], p["draft_tokens"], p["temperature"],
                                     p["u_accept"], p["u_resample"], top_k, top_p, o, nn, w)
 
+    torch.cuda.synchronize()  # inputs built on the default stream are complete
     with torch.cuda.stream(stream):
         st(0)
     torch.cuda.synchronize()
@@ -485,6 +488,7 @@ def multi_workload(sv, dev, stream, steps=1000):
         p = pool[i % len(pool)]
         sv.spec_verify_greedy_multi(p["target"], p["draft_tokens"], o, nn, w, out_choice=ch)
 
+    torch.cuda.synchronize()  # inputs built on the default stream are complete
     with torch.cuda.stream(stream):
         st(0)
     torch.cuda.synchronize()
@@ -535,6 +539,7 @@ def lmhead_workload(sv, dev, stream, steps=200):
     def gemm(i):
         st(i, sv.spec_verify_lmhead_gemm_only)
 
+    torch.cuda.synchronize()  # inputs built on the default stream are complete
     with torch.cuda.stream(stream):
         st(0)
     torch.cuda.synchronize()
@@ -598,6 +603,7 @@ def centroid_workload(sv, dev, stream, steps=500):
         def st(i, hids=hids, ot=ot, ol=ol, oc=oc, ws=ws):
             sv.spec_centroid_head(hids[i % 4], m["centroids"], m["W_ord"], m["cluster_off"], m["ord2tok"], K,
                                   ot, ol, oc, ws)
+        torch.cuda.synchronize()  # inputs built on the default stream are complete
         with torch.cuda.stream(stream):
             st(0)
         torch.cuda.synchronize()
@@ -640,6 +646,7 @@ def centroid_workload(sv, dev, stream, steps=500):
         p, q = pool[i % len(pool)], rounds[i % len(pool)]
         sv.spec_verify_sample_sparse(p["target"], q["tok"], q["lg"], q["cnt"], q["d"], p["temperature"],
                                      p["u_accept"], p["u_resample"], o, n, wsv)
+    torch.cuda.synchronize()  # inputs built on the default stream are complete
     with torch.cuda.stream(stream):
         sp(0)
     torch.cuda.synchronize()

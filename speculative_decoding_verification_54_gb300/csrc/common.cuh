@@ -8,6 +8,7 @@
 #include <cstdint>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <cuda/atomic>
 
 namespace specv {
 
@@ -177,6 +178,19 @@ __device__ __forceinline__ bool seq_is_greedy(const float* temperature, int b) {
   if (temperature == nullptr) return true;
   const float t = temperature[b];
   return !(t > 0.0f);
+}
+
+// The last-CTA handoff of a sequence's tail: every CTA adds one to the
+// sequence's counter with an acquire-release atomic after a barrier (the
+// barrier orders the CTA's writes before thread 0's release); the CTA that
+// brings it to `parts` sees all of them once it has passed the next barrier,
+// and resets the counter for the next call.
+__device__ __forceinline__ bool last_cta_arrives(int* counter, int parts) {
+  cuda::atomic_ref<int, cuda::thread_scope_device> c(*counter);
+  const int old = c.fetch_add(1, cuda::memory_order_acq_rel);
+  const bool last = (old == parts - 1);
+  if (last) c.store(0, cuda::memory_order_relaxed);
+  return last;
 }
 
 // Compensated (Neumaier) summation: s + c carries the sum to about twice the

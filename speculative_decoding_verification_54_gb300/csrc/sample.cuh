@@ -426,15 +426,9 @@ __global__ void __launch_bounds__(kTailThreads, 2) tail_kernel(const __grid_cons
     }
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    const int old = atomicAdd(&p.tail_done[b * kCounterStride], 1);
-    s_last = (old == static_cast<int>(gridDim.x) - 1);
-    if (s_last) p.tail_done[b * kCounterStride] = 0;  // ready for the next call
-  }
+  if (threadIdx.x == 0) s_last = last_cta_arrives(&p.tail_done[b * kCounterStride], gridDim.x);
   __syncthreads();
   if (!s_last) return;
-  __threadfence();
   draw_token<T>(p, b, s, rs, u_res);
 }
 

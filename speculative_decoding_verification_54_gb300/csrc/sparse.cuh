@@ -167,19 +167,17 @@ __device__ __forceinline__ float load_logit(const void* base, size_t idx) {
 // p_n(x) - min(p_n(x), q(x)) with q from the shared-memory map (0 off the
 // candidates); otherwise the plain row's 2^(fma(x, ks, -mk)).
 template <typename T>
-__device__ __forceinline__ int sparse_entry(const SparseParams& p, size_t rowp, int chunk, bool residual,
-                                            const SparseW& f, float plain_mk, const float* qmap, F2 local) {
+__device__ __forceinline__ int sparse_entry(const SparseParams& p, int chunk, bool residual, const SparseW& f,
+                                            float plain_mk, const float* qmap, F2 local, uint4 a) {
   constexpr int P = Elt<T>::kPerVec;
   __shared__ F2 s_wtot[kSparseWarps];
   __shared__ int s_first, s_lastnz, s_tok;
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-  const uint4* vp = chunk_vec<T>(p.target, rowp, p.V, chunk, p.CE);
   const int nvec = min(p.CE, p.V - chunk * p.CE) / P;
   float w[P];
   F2 my = f2_from(0.f);
   int last_nz = -1;
-  {
-    const uint4 a = (t < nvec) ? __ldg(vp + t) : neg_inf_vec<T>();
+  {  // a: vector t of the chunk, loaded by the caller
     float xp[P];
     Elt<T>::unpack(a, xp);
 #pragma unroll
@@ -380,6 +378,15 @@ __global__ void __launch_bounds__(kSparseThreads, 1) sparse_tail_kernel(const __
         const int k = lane + 32 * j;
         v[j] = (k < nvec) ? __ldg(vp + k) : neg_inf_vec<T>();
       }
+      // this lane's first candidate of the chunk, gathered with the vectors
+      // (a chunk holds about 32 candidates: usually the only one)
+      int x0 = -1;
+      float xp0 = 0.f, q0 = 0.f;
+      if (a + lane < e) {
+        x0 = staged ? st_tok[a + lane] : __ldg(tok + lo + a + lane);
+        q0 = staged ? st_q[a + lane] : f.q(__ldg(lg + lo + a + lane));
+        if (x0 >= 0 && x0 < p.V) xp0 = load_logit<T>(p.target, rowp_n * p.V + x0);
+      }
       // compensated (Neumaier) sums per lane, four independent chains;
       // lanes combine in two-float
       float sa[4] = {0.f, 0.f, 0.f, 0.f}, ca[4] = {0.f, 0.f, 0.f, 0.f};
@@ -395,7 +402,8 @@ __global__ void __launch_bounds__(kSparseThreads, 1) sparse_tail_kernel(const __
       for (int k = 0; k < 4; ++k) sp = f2_add(sp, f2_add(f2_from(sa[k]), f2_from(ca[k])));
       // minus min(p_n, q_n) over the chunk's candidates
       float s1 = 0.f, c1m = 0.f;
-      for (int i = a + lane; i < e; i += 32) {
+      if (x0 >= 0 && x0 < p.V) neumaier_add(s1, c1m, fminf(f.p(xp0), q0));
+      for (int i = a + lane + 32; i < e; i += 32) {
         const int x = staged ? st_tok[i] : __ldg(tok + lo + i);
         if (x < 0 || x >= p.V) continue;  // not a token: no weight to take off
         const float q = staged ? st_q[i] : f.q(__ldg(lg + lo + i));
@@ -421,15 +429,9 @@ __global__ void __launch_bounds__(kSparseThreads, 1) sparse_tail_kernel(const __
     }
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    const int old = atomicAdd(&p.tail_done[b * kCounterStride], 1);
-    s_last = (old == static_cast<int>(gridDim.x) - 1);
-    if (s_last) p.tail_done[b * kCounterStride] = 0;
-  }
+  if (threadIdx.x == 0) s_last = last_cta_arrives(&p.tail_done[b * kCounterStride], gridDim.x);
   __syncthreads();
   if (!s_last) return;
-  __threadfence();
 
   // ---- the draw (last CTA): level 1, the chunk ----
   const bool staged_m = p.cpr <= 4096;
@@ -465,6 +467,14 @@ __global__ void __launch_bounds__(kSparseThreads, 1) sparse_tail_kernel(const __
   const int chunk = s_chunk;
   const bool residual = s_resid;
   // ---- level 2: the chunk's candidates scattered into the q map ----
+  const int rowj = (s.mode == kModeResidual) ? s.n : g;  // the Z = 0 fallback keeps row n
+  uint4 av;  // vector t of the chosen chunk: loaded now, used after the map is built
+  {
+    constexpr int P = Elt<T>::kPerVec;
+    const uint4* vp = chunk_vec<T>(p.target, static_cast<size_t>(b) * (g + 1) + rowj, p.V, chunk, p.CE);
+    const int nvec = min(p.CE, p.V - chunk * p.CE) / P;
+    av = (static_cast<int>(threadIdx.x) < nvec) ? __ldg(vp + threadIdx.x) : neg_inf_vec<T>();
+  }
   if (residual) {
     for (int i = threadIdx.x; i < p.CE; i += kSparseThreads) qmap[i] = 0.f;
     __syncthreads();
@@ -475,9 +485,7 @@ __global__ void __launch_bounds__(kSparseThreads, 1) sparse_tail_kernel(const __
     }
     __syncthreads();
   }
-  const int rowj = (s.mode == kModeResidual) ? s.n : g;  // the Z = 0 fallback keeps row n
-  const int e = sparse_entry<T>(p, static_cast<size_t>(b) * (g + 1) + rowj, chunk, residual, f, rs[rowj].mk, qmap,
-                                s_local);
+  const int e = sparse_entry<T>(p, chunk, residual, f, rs[rowj].mk, qmap, s_local, av);
   if (threadIdx.x == 0) p.dp.out_tokens[b * (g + 1) + s.n] = chunk * p.CE + e;
 }
 
