@@ -1,0 +1,82 @@
+"""The multi-GPU path of bench.py on the CPU: replicas only (each rank verifies
+its own batch; no collective on the data path).  The plumbing around the
+timed region -- the barrier, the max of the elapsed time over ranks and the
+whole-job value -- is exercised with world size 2 over gloo, and the
+reference arm's rank rule (rank 0 alone runs and prints) through the
+environment torchrun sets."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _replica(rank, ws, port, elapsed, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(ws),
+                      LOCAL_RANK=str(rank))
+    sys.path.insert(0, ROOT)
+    import bench
+    n, r, local = bench.dist_setup()
+    assert (n, r, local) == (ws, rank, rank)
+    bench.dist_init(n, "gloo")
+    bench.dist_barrier(n)
+    el = bench.dist_max(n, elapsed[rank], "cpu")
+    steps = 100
+    value = n * steps / el  # the whole-job rounds/s the bench reports
+    q.put((rank, el, value))
+    bench.dist_barrier(n)
+    import torch.distributed as dist
+    dist.destroy_process_group()
+
+
+def test_two_replicas_take_the_slowest_rank():
+    torch = pytest.importorskip("torch")
+    import torch.multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    elapsed = [0.25, 0.40]
+    procs = [ctx.Process(target=_replica, args=(r, 2, port, elapsed, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    got = sorted(q.get(timeout=10) for _ in range(2))
+    for rank, el, value in got:
+        assert el == 0.40                      # every rank sees the slowest rank's time
+        assert abs(value - 2 * 100 / 0.40) < 1e-9  # units of all ranks over that time
+
+
+def test_world_size_one_needs_no_process_group():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.dist_max(1, 0.5, "cpu") == 0.5
+    bench.dist_barrier(1)  # no-op
+
+
+def _run_reference(env_extra):
+    env = dict(os.environ, **env_extra)
+    return subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                           "--warmup", "0"], capture_output=True, text=True, env=env, timeout=300, cwd=ROOT)
+
+
+def test_reference_arm_runs_on_rank_zero_only():
+    r1 = _run_reference({"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"})
+    assert r1.returncode == 0 and r1.stdout.strip() == ""
+    r0 = _run_reference({"RANK": "0", "WORLD_SIZE": "2", "LOCAL_RANK": "0"})
+    assert r0.returncode == 0
+    line = json.loads(r0.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle"
+    assert line["e2e"]["h2d_bytes_per_step"] == 0
