@@ -262,7 +262,7 @@ int dispatch(const Common& a, bool sampling) {
 // ---------------------------------------------------------------------------
 struct TkLayout {
   Layout base;  // header (status), the row reducer's partials
-  size_t list_idx, list_val, rowtk, rowd, pre_keys, pre_count, submax, total;
+  size_t list_idx, list_val, rowtk, rowd, submax, total;
 };
 
 TkLayout tk_layout(int B, int gamma, int V) {
@@ -278,10 +278,6 @@ TkLayout tk_layout(int B, int gamma, int V) {
   off += align_up(rows * sizeof(float4), 256);
   L.rowd = off;
   off += align_up(rows * sizeof(float2), 256);
-  L.pre_keys = off;
-  off += align_up(rows * kTkStore * sizeof(unsigned long long), 256);
-  L.pre_count = off;  // zero when no call is running
-  off += align_up(rows * sizeof(int), 256);
   L.submax = off;  // block maxima from the row reducer
   off += align_up(rows * ((static_cast<size_t>(V) + kMinChunk - 1) / kMinChunk) * kVecPerLane * sizeof(float), 256);
   L.total = off;
@@ -327,19 +323,12 @@ int run_topkp(const Common& a, int top_k, float top_p) {
   rp.submax = reinterpret_cast<float*>(ws + L.submax);
   if (launch_pdl(rowstats_kernel<T, kLdg, true>, dim3(pl.grid), dim3(kRowThreads), 0, a.stream, rp) != cudaSuccess)
     return SPEC_ERR_CUDA;
-  // 2. the logits at or above each row's k-th largest block maximum
+  // 2. K and K' per row (K's superset from the block maxima), 3. the
+  // decisions and draws
   k.submax = rp.submax;
-  k.pre_keys = reinterpret_cast<unsigned long long*>(ws + L.pre_keys);
-  k.pre_count = reinterpret_cast<int*>(ws + L.pre_count);
   k.cpr = pl.cpr;
   k.CE = pl.CE;
   const int rows = a.B * (2 * a.gamma + 1);
-  int parts = (2 * dev.sms) / rows;
-  if (parts < 1) parts = 1;
-  if (parts > 8) parts = 8;
-  if (launch_pdl(topk_collect_kernel<T>, dim3(rows, parts), dim3(kTkThreads), 0, a.stream, k) != cudaSuccess)
-    return SPEC_ERR_CUDA;
-  // 3. K and K' per row, 4. the decisions and draws
   if (launch_pdl(topk_select_kernel<T>, dim3(rows), dim3(kTkThreads), 0, a.stream, k) != cudaSuccess)
     return SPEC_ERR_CUDA;
   DecideParams& dp = tp.dp;

@@ -11,12 +11,11 @@
 //        of pk (tie groups stay together; the most likely entries always stay);
 //   p' = softmax over K', 0 elsewhere.
 //
-//   topk_select_kernel  one CTA per row: a radix select of the top_k-th
-//                       largest logit over order-preserving keys (8-bit
-//                       digits from the top, per-warp shared histograms with
-//                       warp-aggregated increments; the first pass reads the
-//                       row from HBM, the later ones mostly from L2), the
-//                       collection of K, a bitonic sort by (logit desc, index
+//   topk_select_kernel  one CTA per row: a superset of K from the row
+//                       reducer's block maxima (the blocks whose maximum
+//                       reaches the top_k-th largest block maximum), else a
+//                       radix select of the top_k-th largest logit over
+//                       order-preserving keys; a sort by (logit desc, index
 //                       asc), the top-p cut from a two-float prefix scan, and
 //                       the kept list re-sorted by vocabulary index.
 //   topkp_tail_kernel   one CTA per sequence: the decision on p'(d)/q'(d)
@@ -51,11 +50,9 @@ struct TopkParams {
   float2* rowd;              // [B*(2*gamma+1)] {logit of the row's draft token, 1 if kept else 0}
   const int32_t* draft_tokens;  // [B, gamma]
   int* status;
-  // the row reducer's chunk partials and the lists topk_collect_kernel fills
-  // from them (nullptr: the select kernel finds K on its own)
-  const float* submax;           // [B*(2*gamma+1)*cpr*kVecPerLane] maxima of 32-vector blocks
-  unsigned long long* pre_keys;  // [B*(2*gamma+1)][kTkStore] (key << 32 | ~index)
-  int* pre_count;                // [B*(2*gamma+1)]; reset to 0 by the select kernel
+  // the maxima of the row reducer's 32-vector blocks, from which the select
+  // kernel bounds K (nullptr: it finds K on its own)
+  const float* submax;  // [B*(2*gamma+1)*cpr*kVecPerLane]
   int B, gamma, V, top_k, cpr, CE;
   float top_p;
 };
@@ -293,16 +290,19 @@ __device__ __forceinline__ int tk_pow2(int n) {
   return p2;
 }
 
-// Block-wide radix select over n keys in shared memory (4 passes of 8-bit
-// digits, most significant first): the k-th largest key (1 <= k <= n).
-// *greater receives how many keys are strictly larger.  All threads call;
-// every thread returns the same.
+// Block-wide radix select over n keys in shared memory (`passes` passes of
+// 8-bit digits, most significant first): the k-th largest key (1 <= k <= n),
+// or, with fewer than 4 passes, its leading 8*passes bits (the rest zero) --
+// exact as a threshold when the keys carry no more significant bits than
+// that, as the keys of bf16 values carry 16.  *greater receives how many keys
+// are strictly larger.  All threads call; every thread returns the same.
 __device__ __forceinline__ uint32_t tk_block_kth(const uint32_t* keys, int n, int k, int* hist, int* s_val,
-                                                 int* greater) {
+                                                 int* greater, int passes = 4) {
   const int t = threadIdx.x;
   uint32_t prefix = 0, mask = 0;
   int remaining = k;
-  for (int shift = 24; shift >= 0; shift -= 8) {
+  for (int pass = 0; pass < passes; ++pass) {
+    const int shift = 24 - 8 * pass;
     for (int i = t; i < 256; i += blockDim.x) hist[i] = 0;
     __syncthreads();
     for (int c = t; c < n; c += blockDim.x) {
@@ -345,45 +345,30 @@ __device__ __forceinline__ uint32_t tk_block_kth(const uint32_t* keys, int n, in
 }
 
 constexpr int kTkCollectMaxBlocks = 4096;  // block maxima held in shared memory
+constexpr int kTkGatherBatch = 8;          // qualifying blocks in flight per warp
+constexpr int kTkRankSortMax = 256;        // longer lists take the bitonic sort
 
-// GPU-wide collection of K's superset, grid (rows, parts).  The row reducer
-// records the maximum of every block of 32 vectors (256 bf16 or 128 fp32
-// logits); those maxima are logits themselves, so the k-th largest of them,
-// M_k, is a lower bound on the k-th largest logit: K lies inside the blocks
-// whose maximum reaches M_k.  The row's CTAs deal those blocks to their warps
-// (one vector per lane) and append the logits >= M_k to the row's list with
-// warp-aggregated atomics (the select kernel sorts, so the order does not
-// matter).  Rows with more than kTkCollectMaxBlocks blocks are left to the
-// select kernel.
+// A superset of K from the row reducer's block maxima.  Those maxima are
+// logits of the row, so the k-th largest of them, M_k, is a lower bound on the
+// k-th largest logit: K lies inside the blocks whose maximum reaches M_k.  The
+// qualifying blocks are compacted in order, the warps gather them
+// kTkGatherBatch at a time (one 16-byte vector per lane) and append every
+// logit >= M_k to sk as (key << 32 | ~index).  Returns how many there are
+// (sk holds the first kTkStore).  `ck` is scratch for kTkCollectMaxBlocks keys
+// and qlist for as many block numbers.
 template <typename T>
-__global__ void __launch_bounds__(kTkThreads, 2) topk_collect_kernel(const __grid_constant__ TopkParams p) {
+__device__ __noinline__ int tk_gather_blocks(const TopkParams& p, int slot, const void* row, int k,
+                                             uint32_t* ck, uint16_t* qlist, int* hist256, int* s_val, int* s_w,
+                                             unsigned long long* sk, int* s_count) {
   constexpr int P = Elt<T>::kPerVec;
-  __shared__ uint32_t ck[kTkCollectMaxBlocks];
-  __shared__ uint16_t qlist[kTkCollectMaxBlocks];  // the qualifying blocks, in order
-  __shared__ int hist[256];
-  __shared__ int s_val[2];
-  __shared__ int s_w[kTkWarps];
-  grid_dep_launch();
-  grid_dep_wait();
-  const int g = p.gamma, slots = 2 * g + 1;
-  const int slot = blockIdx.x, b = slot / slots, t = slot - b * slots;
-  const bool greedy = seq_is_greedy(p.temperature, b);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nb = p.cpr * kVecPerLane;
-  if ((t > g && greedy) || nb > kTkCollectMaxBlocks) return;
-  const int k = greedy ? 1 : min(p.top_k, p.V);
   const float* sm = p.submax + static_cast<size_t>(slot) * nb;
   for (int c = threadIdx.x; c < nb; c += kTkThreads) ck[c] = logit_key(__ldcg(sm + c));
+  if (threadIdx.x == 0) *s_count = 0;
   __syncthreads();
   int greater;  // unused: the list keeps every logit >= the bound
-  const uint32_t thr = (k < nb) ? tk_block_kth(ck, nb, k, hist, s_val, &greater) : 0u;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint8_t* row = (t <= g) ? static_cast<const uint8_t*>(p.target) +
-                                      (static_cast<size_t>(b) * (g + 1) + t) * p.V * sizeof(T)
-                                : static_cast<const uint8_t*>(p.draft) +
-                                      (static_cast<size_t>(b) * g + (t - g - 1)) * p.V * sizeof(T);
-  unsigned long long* out = p.pre_keys + static_cast<size_t>(slot) * kTkStore;
-  int* cnt = p.pre_count + slot;
-  const int nvec_row = p.V / P;
+  const uint32_t thr = (k < nb) ? tk_block_kth(ck, nb, k, hist256, s_val, &greater, sizeof(T) == 2 ? 2 : 4) : 0u;
   // the qualifying blocks, compacted in order: thread t checks blocks
   // [t*per, (t+1)*per), a block scan gives each its position
   const int per = (nb + kTkThreads - 1) / kTkThreads;
@@ -407,56 +392,113 @@ __global__ void __launch_bounds__(kTkThreads, 2) topk_collect_kernel(const __gri
     if (ck[q] >= thr) qlist[before++] = static_cast<uint16_t>(q);
   __syncthreads();
   // block q of chunk c covers the row's vectors c*CE/P + 32j .. +31 (q = 8c + j)
-  const int stride = gridDim.y * kTkWarps;
-  for (int qi = blockIdx.y * kTkWarps + warp; qi < nq; qi += stride) {
-    const int q = qlist[qi];
-    const int c = q / kVecPerLane, j = q - c * kVecPerLane;
-    const int vi = c * (p.CE / P) + 32 * j + lane;  // this lane's vector of the row
-    const bool in = (32 * j + lane) < (p.CE / P) && vi < nvec_row;
-    const uint4 u = in ? __ldg(reinterpret_cast<const uint4*>(row) + vi) : neg_inf_vec<T>();
-    float x[P];
-    Elt<T>::unpack(u, x);
-    uint32_t hits = 0;
+  const uint4* v4 = static_cast<const uint4*>(row);
+  const int nvec_row = p.V / P, vpc = p.CE / P;
+  for (int qb = warp; qb < nq; qb += kTkWarps * kTkGatherBatch) {  // warp-uniform
+    // the batch's loads first (the only registers they hold are the data);
+    // this lane's vector of block q = 8c + j is c*CE/P + 32j + lane
+    uint4 u[kTkGatherBatch];
 #pragma unroll
-    for (int e = 0; e < P; ++e)
-      if (in && logit_key(x[e]) >= thr) hits |= 1u << e;
-    const int nh = __popc(hits);
-    int incl = nh;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int o = __shfl_up_sync(0xffffffffu, incl, off);
-      if (lane >= off) incl += o;
+    for (int j = 0; j < kTkGatherBatch; ++j) {
+      const int qi = qb + j * kTkWarps;
+      const int q = (qi < nq) ? qlist[qi] : 0;
+      const int c = q / kVecPerLane, jb = q - c * kVecPerLane;
+      const int vi = c * vpc + 32 * jb + lane;
+      const bool in = qi < nq && (32 * jb + lane) < vpc && vi < nvec_row;
+      u[j] = in ? __ldg(v4 + vi) : neg_inf_vec<T>();
     }
-    const int total = __shfl_sync(0xffffffffu, incl, 31);
-    if (total == 0) continue;
-    int base = 0;
-    if (lane == 31) base = atomicAdd(cnt, total);
-    base = __shfl_sync(0xffffffffu, base, 31) + incl - nh;
 #pragma unroll
-    for (int e = 0; e < P; ++e) {
-      if ((hits >> e) & 1u) {
-        if (base < kTkStore) {
-          const uint32_t idx = static_cast<uint32_t>(vi * P + e);
-          out[base] = (static_cast<unsigned long long>(logit_key(x[e])) << 32) | (0xffffffffu - idx);
+    for (int j = 0; j < kTkGatherBatch; ++j) {
+      const int qi = qb + j * kTkWarps;
+      if (qi >= nq) break;  // warp-uniform
+      const int q = qlist[qi];
+      const int c = q / kVecPerLane, jb = q - c * kVecPerLane;
+      const int vi = c * vpc + 32 * jb + lane;
+      const bool in = (32 * jb + lane) < vpc && vi < nvec_row;
+      float x[P];
+      Elt<T>::unpack(u[j], x);
+      uint32_t hits = 0;
+#pragma unroll
+      for (int e = 0; e < P; ++e)
+        if (in && logit_key(x[e]) >= thr) hits |= 1u << e;
+      const int nh = __popc(hits);
+      int inc = nh;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, inc, off);
+        if (lane >= off) inc += o;
+      }
+      const int total = __shfl_sync(0xffffffffu, inc, 31);
+      if (total == 0) continue;  // warp-uniform
+      int base = 0;
+      if (lane == 31) base = atomicAdd(s_count, total);
+      base = __shfl_sync(0xffffffffu, base, 31) + inc - nh;
+#pragma unroll
+      for (int e = 0; e < P; ++e) {
+        if ((hits >> e) & 1u) {
+          if (base < kTkStore) {
+            const uint32_t idx = static_cast<uint32_t>(vi * P + e);
+            sk[base] = (static_cast<unsigned long long>(logit_key(x[e])) << 32) | (0xffffffffu - idx);
+          }
+          ++base;
         }
-        ++base;
       }
     }
   }
+  __syncthreads();
+  return *s_count;
+}
+
+// Sort of n distinct 64-bit keys in shared memory, descending.  Up to
+// kTkRankSortMax keys: each key goes to its rank (the number of larger keys)
+// in tmp and back, one pass.  Longer lists: padded with zeros to a power of
+// two and sorted by tk_sort_desc (the zeros end up behind the n keys).
+__device__ __forceinline__ void tk_sort_keys_desc(unsigned long long* a, int n, unsigned long long* tmp) {
+  if (n <= kTkRankSortMax) {
+    for (int i = threadIdx.x; i < n; i += kTkThreads) {
+      const unsigned long long x = a[i];
+      int r = 0;
+#pragma unroll 4
+      for (int j = 0; j < n; ++j) r += (a[j] > x) ? 1 : 0;
+      tmp[r] = x;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < n; i += kTkThreads) a[i] = tmp[i];
+    __syncthreads();
+    return;
+  }
+  const int n2 = tk_pow2(n);
+  for (int i = n + threadIdx.x; i < n2; i += kTkThreads) a[i] = 0ull;
+  __syncthreads();
+  tk_sort_desc(a, n2);
+  __syncthreads();
 }
 
 template <typename T>
 __global__ void __launch_bounds__(kTkThreads, 2) topk_select_kernel(const __grid_constant__ TopkParams p) {
   constexpr int P = Elt<T>::kPerVec;
-  __shared__ int hist[kTkWarps * 256];
+  // hist (the radix select's per-warp histograms) is also the block-maximum
+  // keys while K's superset is gathered, and the sort's scratch afterwards
+  __shared__ __align__(16) int hist[kTkWarps * 256];
   __shared__ unsigned long long sk[kTkStore];
+  __shared__ uint16_t qlist[kTkCollectMaxBlocks];
+  __shared__ int hist256[256];
   __shared__ F2 s_wtot[kTkWarps];
+  __shared__ int s_val[2], s_w[kTkWarps];
   __shared__ int s_digit, s_remaining, s_count, s_cut;
+  static_assert(kTkWarps * 256 * sizeof(int) >= kTkCollectMaxBlocks * sizeof(uint32_t), "block-maximum keys");
+  static_assert(kTkWarps * 256 * sizeof(int) >= kTkStore * sizeof(unsigned long long), "sort scratch");
+  unsigned long long* sort_tmp = reinterpret_cast<unsigned long long*>(hist);
   grid_dep_launch();
-  grid_dep_wait();  // the collection kernel's lists
   const int g = p.gamma, slots = 2 * g + 1;
   const int slot = blockIdx.x, b = slot / slots, t = slot - b * slots;
+  // inputs of the call, read before the wait for the row reducer
   const bool greedy = seq_is_greedy(p.temperature, b);
+  const float temp = p.temperature[b];
+  // the draft token this row is checked against (target row t < gamma and
+  // draft row t - gamma - 1 both check d_{t+1})
+  const int dtok = (t == g) ? -1 : p.draft_tokens[b * g + (t < g ? t : t - g - 1)];
+  grid_dep_wait();  // the row reducer's block maxima
   if (t > g && greedy) return;  // greedy sequences read no draft rows
   const void* row = (t <= g) ? static_cast<const void*>(static_cast<const T*>(p.target) +
                                                         (static_cast<size_t>(b) * (g + 1) + t) * p.V)
@@ -465,23 +507,20 @@ __global__ void __launch_bounds__(kTkThreads, 2) topk_select_kernel(const __grid
   const int k = greedy ? 1 : min(p.top_k, p.V);
 
   // ---- K (or a superset of it) into shared memory ----
-  // Usually one pass: a threshold from the sample (its rank-s largest entry,
-  // s = k/8 + 8, sits above about 2k + 128 entries of the row), then the
-  // entries reaching it.  If that misses (fewer than k entries, or more than
-  // the list holds), the exact radix select over the whole row.
+  // Usually from the block maxima.  Without them, or if that list is not
+  // usable (fewer than k entries cannot happen; more than kTkStore can), a
+  // threshold from a sample (its rank-s largest entry, s = k/8 + 8, sits
+  // above about 2k + 128 entries of the row), then the entries reaching it;
+  // if that misses too, the exact radix select over the whole row.
   const TkRange<T> full{p.V / P, false}, smp{p.V / P, true};
   const int srank = k / 8 + 8;
   uint32_t prefix = 0, pmask = 0;
   int count = -1;
-  if (p.pre_count != nullptr) {  // the list topk_collect_kernel gathered, if it is complete
-    const int pc = __ldcg(p.pre_count + slot);
-    if (pc >= k && pc <= kTkStore) {
-      const unsigned long long* pk = p.pre_keys + static_cast<size_t>(slot) * kTkStore;
-      for (int i = threadIdx.x; i < pc; i += kTkThreads) sk[i] = __ldcg(pk + i);
-      count = pc;
-    }
+  if (p.submax != nullptr && p.cpr * kVecPerLane <= kTkCollectMaxBlocks) {
+    count = tk_gather_blocks<T>(p, slot, row, k, reinterpret_cast<uint32_t*>(hist), qlist, hist256, s_val, s_w, sk,
+                                &s_count);
+    if (count < k || count > kTkStore) count = -1;
     __syncthreads();
-    if (threadIdx.x == 0) p.pre_count[slot] = 0;  // ready for the next call
   }
   if (count < 0 && p.V >= 4096 && srank <= smp.count()) {
     tk_radix_select<T>(row, smp, srank, hist, &s_digit, &s_remaining, &prefix, &pmask);
@@ -497,10 +536,7 @@ __global__ void __launch_bounds__(kTkThreads, 2) topk_select_kernel(const __grid
     if (threadIdx.x == 0) atomicOr(p.status, kStatusTopkOverflow);
     count = kTkStore;
   }
-  const int n2 = tk_pow2(count);
-  for (int i = count + threadIdx.x; i < n2; i += kTkThreads) sk[i] = 0ull;
-  __syncthreads();
-  tk_sort_desc(sk, n2);  // logit descending, index ascending
+  tk_sort_keys_desc(sk, count, sort_tmp);  // logit descending, index ascending
   {
     // K: the entries whose key reaches the k-th largest (the collection may
     // hold a superset); ties with the k-th stay
@@ -520,7 +556,7 @@ __global__ void __launch_bounds__(kTkThreads, 2) topk_select_kernel(const __grid
   }
 
   // ---- softmax over K, the top-p cut, the normaliser of K' ----
-  const float ks = kLog2e / p.temperature[b];
+  const float ks = kLog2e / temp;
   const float mk = key_logit(static_cast<uint32_t>(sk[0] >> 32)) * ks;
   float e[4];
   uint32_t kj[4];
@@ -574,19 +610,16 @@ __global__ void __launch_bounds__(kTkThreads, 2) topk_select_kernel(const __grid
     }
   }
   __syncthreads();
-  const int c2 = tk_pow2(cut);
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     const int j = 4 * threadIdx.x + q;
-    if (j < c2) sk[j] = mine[q];  // entries >= cut are the padding zeros
+    if (j < cut) sk[j] = mine[q];
   }
   __syncthreads();
-  tk_sort_desc(sk, c2);  // index ascending
+  tk_sort_keys_desc(sk, cut, sort_tmp);  // index ascending
   int* li = p.list_idx + static_cast<size_t>(slot) * kTkStore;
   float* lv = p.list_val + static_cast<size_t>(slot) * kTkStore;
-  // the draft token this row is checked against (target row t < gamma and
-  // draft row t - gamma - 1 both check d_{t+1}); its logit if it was kept
-  const int dtok = (t == g) ? -1 : p.draft_tokens[b * g + (t < g ? t : t - g - 1)];
+  // the logit of the row's draft token if it was kept
   if (threadIdx.x == 0) p.rowd[slot] = make_float2(0.f, 0.f);
   __syncthreads();
   for (int j = threadIdx.x; j < cut; j += kTkThreads) {
@@ -632,13 +665,21 @@ __global__ void __launch_bounds__(kTkThreads, 1) topkp_tail_kernel(const __grid_
   const int b = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = dp.gamma, slots = 2 * g + 1;
   const bool greedy = seq_is_greedy(dp.temperature, b);
+  // inputs of the call, read before the wait for the select kernel
+  const float ks = greedy ? 0.f : kLog2e / dp.temperature[b];
+  const float u_res = p.u_resample[b];
+  int d = -1;
+  float u_acc = 0.f;
+  if (warp == 0 && lane < g) {
+    d = dp.draft_tokens[b * g + lane];
+    u_acc = dp.u_accept[b * g + lane];
+  }
   grid_dep_wait();
   for (int r = threadIdx.x; r < (greedy ? g + 1 : slots); r += kTkThreads) {
     rt[r] = __ldcg(tk.rowtk + b * slots + r);
     rd[r] = __ldcg(tk.rowd + b * slots + r);
   }
   __syncthreads();
-  const float ks = greedy ? 0.f : kLog2e / dp.temperature[b];
   auto list_idx = [&](int r) { return tk.list_idx + static_cast<size_t>(b * slots + r) * kTkStore; };
   auto list_val = [&](int r) { return tk.list_val + static_cast<size_t>(b * slots + r) * kTkStore; };
   auto count_of = [&](int r) { return __float_as_int(rt[r].x); };
@@ -646,10 +687,8 @@ __global__ void __launch_bounds__(kTkThreads, 1) topkp_tail_kernel(const __grid_
   // ---- decision: one lane per draft position ----
   if (warp == 0) {
     bool acc = false;
-    int d = -1;
     float pp = 0.f, qq = 0.f;
     if (lane < g) {
-      d = dp.draft_tokens[b * g + lane];
       const bool valid = d >= 0 && d < dp.V;
       if (!valid) atomicOr(dp.status, kStatusBadToken);
       if (valid && greedy) {
@@ -664,7 +703,7 @@ __global__ void __launch_bounds__(kTkThreads, 1) topkp_tail_kernel(const __grid_
         if (!hq) rho = INFINITY;      // q'(d) = 0: accepted
         else if (!hp) rho = 0.f;      // p'(d) = 0, q'(d) > 0: rejected
         else rho = ex2((dp_.x - dq_.x) * ks - (rp.y - rq.y) - (rp.z - rq.z));
-        acc = dp.u_accept[b * g + lane] < rho;
+        acc = u_acc < rho;
       }
     }
     const unsigned rej = ~__ballot_sync(0xffffffffu, acc) & ((1u << g) - 1u);
@@ -707,6 +746,16 @@ __global__ void __launch_bounds__(kTkThreads, 1) topkp_tail_kernel(const __grid_
   const float4 rq = residual ? rt[g + 1 + n] : make_float4(0.f, 0.f, 0.f, 0.f);
   const float invSp = ex2(-rp.z), invSq = ex2(-rq.z);
   const int cq = residual ? count_of(g + 1 + n) : 0;
+  // this thread's entries 4t .. 4t+3 of row r's list (ascending vocabulary
+  // index), loaded while the draft row's list is staged
+  int ix[4];
+  float lx[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int j = 4 * threadIdx.x + q;
+    ix[q] = (j < cnt) ? __ldcg(li + j) : -1;
+    lx[q] = (j < cnt) ? __ldcg(lv + j) : 0.f;
+  }
   if (residual) {  // the draft row's kept list, searched from shared memory
     for (int j = threadIdx.x; j < cq; j += kTkThreads) {
       sq_idx[j] = __ldcg(list_idx(g + 1 + n) + j);
@@ -715,16 +764,13 @@ __global__ void __launch_bounds__(kTkThreads, 1) topkp_tail_kernel(const __grid_
     __syncthreads();
   }
   float w[4], wp[4];
-  int ix[4];
   F2 my = f2_from(0.f), myp = f2_from(0.f);
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {  // entries 4t .. 4t+3, ascending vocabulary index
+  for (int q = 0; q < 4; ++q) {
     const int j = 4 * threadIdx.x + q;
-    ix[q] = -1;
     w[q] = wp[q] = 0.f;
     if (j < cnt) {
-      ix[q] = __ldcg(li + j);
-      wp[q] = ex2(fmaf(__ldcg(lv + j), ks, -rp.y)) * invSp;
+      wp[q] = ex2(fmaf(lx[q], ks, -rp.y)) * invSp;
       w[q] = wp[q];
       if (residual) {
         const int iq = tk_find(sq_idx, cq, ix[q]);
@@ -744,7 +790,7 @@ __global__ void __launch_bounds__(kTkThreads, 1) topkp_tail_kernel(const __grid_
     my = myp;
     incl = tk_block_scan(my, s_wtot, &Z);
   }
-  const F2 target = f2_mul_f(Z, p.u_resample[b]);
+  const F2 target = f2_mul_f(Z, u_res);
   if (f2_gt(incl, target)) atomicMin(&s_first, static_cast<int>(threadIdx.x));
   int last_nz = -1;
 #pragma unroll
@@ -762,7 +808,11 @@ __global__ void __launch_bounds__(kTkThreads, 1) topkp_tail_kernel(const __grid_
     }
     if (j < 0) j = last_nz;  // rounding inside the thread: its last nonzero entry
     if (j < 0) j = 4 * threadIdx.x;  // (the crossing thread always holds weight; kept in bounds regardless)
-    dp.out_tokens[b * (g + 1) + n] = __ldcg(li + j);
+    int tok = -1;
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (4 * static_cast<int>(threadIdx.x) + q == j) tok = ix[q];
+    dp.out_tokens[b * (g + 1) + n] = tok >= 0 ? tok : __ldcg(li + j);
   } else if (threadIdx.x == 0 && s_first == INT_MAX) {
     // beyond the total (rounding): the last entry of nonzero weight
     const int j = s_lastnz < 0 ? 0 : s_lastnz;
