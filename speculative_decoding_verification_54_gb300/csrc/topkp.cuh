@@ -91,24 +91,30 @@ __device__ __forceinline__ void tk_histogram(const void* row, const TkRange<T>& 
                                              int shift, int* hist /* [kTkWarps][256] */) {
   constexpr int P = Elt<T>::kPerVec;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int kBatch = 4;  // vectors in flight per thread
   const uint4* v4 = reinterpret_cast<const uint4*>(row);
   const int n = rg.count();
   int* h = hist + warp * 256;
-  for (int i = threadIdx.x; i - lane < n; i += kTkThreads) {  // whole warps iterate together
-    float x[P];
-    if (i < n) {
-      Elt<T>::unpack(__ldg(v4 + rg.vec(i)), x);
-    } else {
+  for (int base = 0; base < n; base += kBatch * kTkThreads) {  // block-uniform
+    uint4 u[kBatch];
 #pragma unroll
-      for (int k = 0; k < P; ++k) x[k] = -INFINITY;
+    for (int j = 0; j < kBatch; ++j) {
+      const int i = base + j * kTkThreads + threadIdx.x;
+      u[j] = (i < n) ? __ldg(v4 + rg.vec(i)) : neg_inf_vec<T>();
     }
 #pragma unroll
-    for (int k = 0; k < P; ++k) {
-      const uint32_t key = logit_key(x[k]);
-      const bool in = (i < n) && ((key & pmask) == prefix);
-      const int digit = in ? static_cast<int>((key >> shift) & 255u) : 256;
-      const unsigned same = __match_any_sync(0xffffffffu, digit);
-      if (in && lane == __ffs(same) - 1) atomicAdd(&h[digit], __popc(same));
+    for (int j = 0; j < kBatch; ++j) {
+      const int i = base + j * kTkThreads + threadIdx.x;
+      float x[P];
+      Elt<T>::unpack(u[j], x);
+#pragma unroll
+      for (int k = 0; k < P; ++k) {
+        const uint32_t key = logit_key(x[k]);
+        const bool in = (i < n) && ((key & pmask) == prefix);
+        const int digit = in ? static_cast<int>((key >> shift) & 255u) : 256;
+        const unsigned same = __match_any_sync(0xffffffffu, digit);
+        if (in && lane == __ffs(same) - 1) atomicAdd(&h[digit], __popc(same));
+      }
     }
   }
 }
@@ -178,62 +184,69 @@ __device__ __noinline__ void tk_radix_select(const void* row, const TkRange<T>& 
 
 // Every entry of the row whose significant key bits reach (prefix, pmask),
 // packed (key, ~index) into sk (at most kTkStore kept); returns the count of
-// all such entries.  A vector is looked at element by element only when its
-// maximum reaches the threshold.
-// The entries of one 16-byte vector that reach the threshold, appended to sk
-// (warp-wide; only called for vectors where some lane has a hit).
-template <typename T>
-__device__ __noinline__ void tk_collect_vec(uint4 u, int i, int nvec, uint32_t prefix, uint32_t pmask,
-                                            unsigned long long* sk, int* s_count) {
-  constexpr int P = Elt<T>::kPerVec;
-  const int lane = threadIdx.x & 31;
-  float x[P];
-  Elt<T>::unpack(u, x);
-#pragma unroll 1
-  for (int q = 0; q < P; ++q) {
-    const uint32_t key = logit_key(x[q]);
-    const bool in = (i < nvec) && ((key & pmask) >= prefix);
-    const unsigned m = __ballot_sync(0xffffffffu, in);
-    if (m == 0u) continue;
-    int b0 = 0;
-    if (lane == 0) b0 = atomicAdd(s_count, __popc(m));
-    b0 = __shfl_sync(0xffffffffu, b0, 0);
-    if (in) {
-      const int pos = b0 + __popc(m & ((1u << lane) - 1u));
-      const uint32_t idx = static_cast<uint32_t>(i * P + q);
-      if (pos < kTkStore) sk[pos] = (static_cast<unsigned long long>(key) << 32) | (0xffffffffu - idx);
-    }
-  }
-}
-
+// all such entries.  Each thread marks the hits of its batch of vectors in a
+// bit mask (a vector is looked at element by element only when its maximum
+// reaches the threshold); one warp scan and one shared-memory atomic per
+// batch place them.
 template <typename T>
 __device__ __noinline__ int tk_collect(const void* row, int V, uint32_t prefix, uint32_t pmask,
                                        unsigned long long* sk, int* s_count) {
   constexpr int P = Elt<T>::kPerVec;
   constexpr int kBatch = 8;  // vectors in flight per thread
+  static_assert(kBatch * P <= 64, "hit mask");
+  const int lane = threadIdx.x & 31;
   const uint4* v4 = reinterpret_cast<const uint4*>(row);
   const int nvec = V / P;
   if (threadIdx.x == 0) *s_count = 0;
   __syncthreads();
-  for (int base = 0; base < nvec; base += kBatch * kTkThreads) {
+  for (int base = 0; base < nvec; base += kBatch * kTkThreads) {  // block-uniform
     uint4 u[kBatch];
 #pragma unroll
     for (int j = 0; j < kBatch; ++j) {
       const int i = base + j * kTkThreads + threadIdx.x;
       u[j] = (i < nvec) ? __ldg(v4 + i) : neg_inf_vec<T>();
     }
-    unsigned hits = 0u;
+    unsigned long long hits = 0ull;
 #pragma unroll
-    for (int j = 0; j < kBatch; ++j)
-      if ((logit_key(vec_max<T>(u[j])) & pmask) >= prefix) hits |= 1u << j;
-    unsigned any = __reduce_or_sync(0xffffffffu, hits);
-    while (any) {  // warp-uniform: the vectors of the batch where some lane has a hit
-      const int j = __ffs(any) - 1;
-      any &= any - 1u;
-      uint4 uj = u[0];
+    for (int j = 0; j < kBatch; ++j) {
+      const bool inb = base + j * kTkThreads + static_cast<int>(threadIdx.x) < nvec;
+      if (inb && (logit_key(vec_max<T>(u[j])) & pmask) >= prefix) {
+        float x[P];
+        Elt<T>::unpack(u[j], x);
 #pragma unroll
-      for (int jj = 1; jj < kBatch; ++jj) uj = (jj == j) ? u[jj] : uj;
-      tk_collect_vec<T>(uj, base + j * kTkThreads + threadIdx.x, nvec, prefix, pmask, sk, s_count);
+        for (int e = 0; e < P; ++e)
+          if ((logit_key(x[e]) & pmask) >= prefix) hits |= 1ull << (j * P + e);
+      }
+    }
+    const int nh = __popcll(hits);
+    int inc = nh;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, inc, off);
+      if (lane >= off) inc += o;
+    }
+    const int total = __shfl_sync(0xffffffffu, inc, 31);
+    if (total == 0) continue;  // warp-uniform
+    int pos = 0;
+    if (lane == 31) pos = atomicAdd(s_count, total);
+    pos = __shfl_sync(0xffffffffu, pos, 31) + inc - nh;
+    while (hits) {
+      const int bit = __ffsll(static_cast<long long>(hits)) - 1;
+      hits &= hits - 1ull;
+      const int j = bit / P, e = bit - j * P;
+      if (pos < kTkStore) {
+        uint4 uj = u[0];
+#pragma unroll
+        for (int jj = 1; jj < kBatch; ++jj) uj = (jj == j) ? u[jj] : uj;
+        float x[P];
+        Elt<T>::unpack(uj, x);
+        float xe = x[0];
+#pragma unroll
+        for (int ee = 1; ee < P; ++ee) xe = (ee == e) ? x[ee] : xe;
+        const uint32_t idx = static_cast<uint32_t>((base + j * kTkThreads + threadIdx.x) * P + e);
+        sk[pos] = (static_cast<unsigned long long>(logit_key(xe)) << 32) | (0xffffffffu - idx);
+      }
+      ++pos;
     }
   }
   __syncthreads();
@@ -250,7 +263,8 @@ __device__ __forceinline__ void tk_sort_desc(unsigned long long* a, int n_pow2) 
   for (int size = 2; size <= n_pow2; size <<= 1) {
     for (int stride = size >> 1; stride > 0; stride >>= 1) {
       for (int i = threadIdx.x; i < n_pow2 / 2; i += kTkThreads) {
-        const int lo = (i / stride) * stride * 2 + (i % stride), hi = lo + stride;
+        // (i / stride) * 2 * stride + i % stride, stride a power of two
+        const int lo = ((i & ~(stride - 1)) << 1) | (i & (stride - 1)), hi = lo + stride;
         const bool desc = ((lo & size) == 0);
         const unsigned long long x = a[lo], y = a[hi];
         if ((x < y) == desc) {
@@ -368,7 +382,7 @@ __device__ __noinline__ int tk_gather_blocks(const TopkParams& p, int slot, cons
   if (threadIdx.x == 0) *s_count = 0;
   __syncthreads();
   int greater;  // unused: the list keeps every logit >= the bound
-  const uint32_t thr = (k < nb) ? tk_block_kth(ck, nb, k, hist256, s_val, &greater, sizeof(T) == 2 ? 2 : 4) : 0u;
+  const uint32_t thr = tk_block_kth(ck, nb, k, hist256, s_val, &greater, sizeof(T) == 2 ? 2 : 4);  // k < nb
   // the qualifying blocks, compacted in order: thread t checks blocks
   // [t*per, (t+1)*per), a block scan gives each its position
   const int per = (nb + kTkThreads - 1) / kTkThreads;
@@ -509,24 +523,38 @@ __global__ void __launch_bounds__(kTkThreads, 2) topk_select_kernel(const __grid
   // ---- K (or a superset of it) into shared memory ----
   // Usually from the block maxima.  Without them, or if that list is not
   // usable (fewer than k entries cannot happen; more than kTkStore can), a
-  // threshold from a sample (its rank-s largest entry, s = k/8 + 8, sits
-  // above about 2k + 128 entries of the row), then the entries reaching it;
-  // if that misses too, the exact radix select over the whole row.
+  // threshold from a sample (its rank-s largest entry sits above about 16 s
+  // entries of the row; s = k/8 + 8, about 2k + 128, capped so that 16 s
+  // stays well inside the kept list), then the entries reaching it; if that
+  // misses too, the exact radix select over the whole row.
   const TkRange<T> full{p.V / P, false}, smp{p.V / P, true};
-  const int srank = k / 8 + 8;
+  const int srank = min(k / 8 + 8, (kTkStore * 4 / 5) / 16);
   uint32_t prefix = 0, pmask = 0;
   int count = -1;
-  if (p.submax != nullptr && p.cpr * kVecPerLane <= kTkCollectMaxBlocks) {
+  // (with k at least the number of blocks the bound would keep every logit)
+  if (p.submax != nullptr && k < p.cpr * kVecPerLane && p.cpr * kVecPerLane <= kTkCollectMaxBlocks) {
     count = tk_gather_blocks<T>(p, slot, row, k, reinterpret_cast<uint32_t*>(hist), qlist, hist256, s_val, s_w, sk,
                                 &s_count);
     if (count < k || count > kTkStore) count = -1;
     __syncthreads();
   }
-  if (count < 0 && p.V >= 4096 && srank <= smp.count()) {
-    tk_radix_select<T>(row, smp, srank, hist, &s_digit, &s_remaining, &prefix, &pmask);
-    count = tk_collect<T>(row, p.V, prefix, pmask, sk, &s_count);
-    if (count < k || count > kTkStore) count = -1;
-    __syncthreads();
+  if (count < 0 && p.V >= 4096) {
+    // a miss gives the row's true count for that rank: the next rank is
+    // scaled toward the middle of [k, kTkStore] (two more tries at most)
+    int sr = srank;
+#pragma unroll 1
+    for (int attempt = 0; attempt < 3 && sr >= 1 && sr <= smp.count(); ++attempt) {
+      tk_radix_select<T>(row, smp, sr, hist, &s_digit, &s_remaining, &prefix, &pmask);
+      const int c = tk_collect<T>(row, p.V, prefix, pmask, sk, &s_count);
+      __syncthreads();
+      if (c >= k && c <= kTkStore) {
+        count = c;
+        break;
+      }
+      const int want = (k + kTkStore) / 2;
+      const int next = static_cast<int>(static_cast<long long>(sr) * want / max(c, 1));
+      sr = (next != sr) ? next : (c > kTkStore ? sr - 1 : sr + 1);
+    }
   }
   if (count < 0) {
     tk_radix_select<T>(row, full, k, hist, &s_digit, &s_remaining, &prefix, &pmask);

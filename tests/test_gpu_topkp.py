@@ -88,6 +88,18 @@ def test_topkp_bf16_full_vocab_batched(sv):
     assert x <= 1
 
 
+@pytest.mark.parametrize("top_k,top_p", [(1024, 1.0), (300, 0.8)])
+def test_topkp_bf16_full_vocab_large_k(sv, top_k, top_p):
+    """k at or above the number of 256-entry blocks of a 262,144-entry row
+    (1,024: the block maxima bound nothing, so K comes from the sampled
+    threshold) and a k below it with a deep top-p cut."""
+    inp = wl.make_round("batched", 1)
+    out, num, dbg, st = _run(sv, inp, top_k, top_p)
+    assert st == sv.SPEC_OK
+    e, x = _compare(inp, top_k, top_p, out, num, dbg, seqs=[2, 13, 29])
+    assert x <= 1
+
+
 def test_topkp_fp32_mixed_greedy(sv):
     inp = wl.make_custom(16, 8, 262144, "f32", "zipf", sigma=("uniform", 0.1, 1.5),
                          temperature=("alternate", 0.0, 1.0), seed=3)
