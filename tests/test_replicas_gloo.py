@@ -3,7 +3,8 @@ its own batch; no collective on the data path).  The plumbing around the
 timed region -- the barrier, the max of the elapsed time over ranks and the
 whole-job value -- is exercised with world size 2 over gloo, and the
 reference arm's rank rule (rank 0 alone runs and prints) through the
-environment torchrun sets."""
+environment torchrun sets.  The CPU baseline's pool of spawned oracle
+workers is run on a small round."""
 import json
 import os
 import socket
@@ -80,3 +81,18 @@ def test_reference_arm_runs_on_rank_zero_only():
     assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle"
     assert line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_oracle_pool_on_all_cores_runs_every_task():
+    """The all-cores oracle leg of the bench's cpu_baseline: spawned workers
+    attach the round's logits (fp32 here, bf16 in the bench) from shared
+    memory and verify one sequence per task; every task completes and the
+    shared blocks are released."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import workloads as wl
+    inp = wl.make_round("tiny", 0)
+    h = dict(target=inp.target, draft=inp.draft, draft_tokens=inp.draft_tokens, temperature=inp.temperature,
+             u_accept=inp.u_accept, u_resample=inp.u_resample)
+    n, el = bench._oracle_all_cores(h, 6, 2)
+    assert n == 6 and el > 0
