@@ -21,7 +21,10 @@
 //   warps 3-10 two groups of four (one warp per TMEM lane quadrant) take
 //              alternate accumulator chunks.  The accumulator rotates through
 //              512/chunk TMEM slots, so the epilogue of one chunk overlaps the
-//              MMAs of the next.
+//              MMAs of the next;
+//   warps 11-14 the row reducer's work for the draft rows (their chunk
+//              statistics), streamed from HBM beside the GEMM, which leaves
+//              most of the HBM bandwidth idle.
 // The epilogue holds, per thread, one vocabulary entry's logits for 32 rows at
 // a time.  Per-row statistics over the tile's 128 entries come from a warp
 // reduce-scatter (shuffles) followed by a combine of the four quadrant warps
@@ -38,6 +41,7 @@
 #include <cuda.h>
 
 #include "common.cuh"
+#include "rowstats.cuh"
 #include "tc.cuh"
 
 namespace specv {
@@ -49,8 +53,10 @@ constexpr int kLmMaxChunk = 256;    // MMA N limit
 constexpr uint32_t kLmWBytes = kLmTileV * kLmTileK * 2;  // 16 KB
 constexpr int kLmMaxWStages = 6, kLmMaxHStages = 6, kLmMaxSlots = 4;
 constexpr int kLmWPrefetch = 12;  // W steps prefetched into L2 ahead of the ring (192 KB per CTA)
-constexpr int kLmEpiGroups = 2;                           // of four warps
-constexpr int kLmThreads = 32 * (3 + 4 * kLmEpiGroups);   // 352
+constexpr int kLmEpiGroups = 2;                                         // of four warps
+constexpr int kLmRowWarp0 = 3 + 4 * kLmEpiGroups;                       // first row warp
+constexpr int kLmRowWarps = 4;                                          // the draft rows' statistics
+constexpr int kLmThreads = 32 * (kLmRowWarp0 + kLmRowWarps);            // 480
 constexpr uint32_t kLmTmemCols = 512;
 
 struct LmParams {
@@ -64,6 +70,10 @@ struct LmParams {
   float4* partials;           // [R][n_tiles] {M, s, argmax bits, mk}
   float* logits;              // [B, gamma, V] fp32, rows j < gamma of sampling sequences
   int* status;
+  // the draft rows' chunk statistics (the row reducer's items, target rows
+  // skipped), computed by the row warps beside the GEMM; rows.draft ==
+  // nullptr: none
+  RowStatsParams rows;
 };
 
 // Dynamic shared memory: W ring, hidden ring, per epilogue group the
@@ -447,7 +457,7 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_kernel(const __grid_cons
         if (p.n_chunks > 1) tc_commit(&sfull[dslot[1]]);
       }
     }
-  } else {
+  } else if (warp < kLmRowWarp0) {
     // ---------------- epilogue: warps 3..10, two groups of four ----------------
     const int e = warp - 3, grp = e >> 2, quad = warp & 3;
     LmEpiScratch S;
@@ -472,12 +482,34 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_kernel(const __grid_cons
       const uint32_t tacc = tmem + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(slot * p.nc);
       lm_epilogue_chunk(p, T, S, tacc, tile, c, quad, lane, 1 + grp, &sempty[slot]);
     }
+  } else {
+    // ---------------- row warps: the draft rows' chunk statistics ----------------
+    // The row reducer's items (one 4 KB chunk of a draft row per warp and
+    // step), dealt over the grid's row warps.  The draft logits are inputs of
+    // the call, so this streaming overlaps the GEMM: it takes HBM bandwidth
+    // the W stream leaves idle.
+    const RowStatsParams& rp = p.rows;
+    if (rp.draft != nullptr) {
+      const int n_slots = rp.B * (2 * rp.gamma + 1);
+      ItemIter it;
+      it.init(static_cast<int>(blockIdx.x) * kLmRowWarps + (warp - kLmRowWarp0),
+              static_cast<int>(gridDim.x) * kLmRowWarps, rp.cpr);
+      Item d;
+      while (next_live<__nv_bfloat16>(rp, it, n_slots, d)) {
+        uint4 v[kVecPerLane];
+#pragma unroll
+        for (int j = 0; j < kVecPerLane; ++j) {
+          const int k = lane + 32 * j;
+          v[j] = (k < d.nvec) ? ld_stream(d.src + k) : neg_inf_vec<__nv_bfloat16>();
+        }
+        finish_item<__nv_bfloat16, false>(rp, d, v, lane);
+      }
+    }
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   if (warp == 2) tmem_dealloc(tmem, kLmTmemCols);
-  grid_dep_wait();  // the row reducer launched before this kernel has finished too
 }
 
 }  // namespace specv

@@ -484,7 +484,8 @@ int run_lm_chain(const LmArgs& a) {
   int* status = reinterpret_cast<int*>(ws + L.base.header);
   const int R = a.B * (a.gamma + 1);
 
-  // 1. draft rows: chunk partials (the row reducer, target rows skipped)
+  // 1. draft rows: chunk partials (the row reducer's items, target rows
+  // skipped), computed by the GEMM kernel's row warps
   const Plan pl = make_plan_rows(a.B * a.gamma, a.V, sizeof(__nv_bfloat16), dev.sms, kLdg);
   RowStatsParams rp = {};
   rp.target = nullptr;
@@ -498,12 +499,8 @@ int run_lm_chain(const LmArgs& a) {
   rp.CE = pl.CE;
   rp.cpr = pl.cpr;
   rp.draft_only = 1;
-  if (!a.gemm_only) {
-    rowstats_kernel<__nv_bfloat16, kLdg><<<pl.grid, kRowThreads, 0, a.stream>>>(rp);
-    if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
-  }
 
-  // 2. target rows: the lm_head GEMM with its statistics epilogue
+  // 2. target rows: the lm_head GEMM with its statistics epilogue (same kernel)
   LmPlan plan;
   if (!lm_plan(R, dev.lm_max_dyn, &plan)) return SPEC_ERR_UNSUPPORTED;
   LmParams lp;
@@ -525,13 +522,16 @@ int run_lm_chain(const LmArgs& a) {
   lp.partials = reinterpret_cast<float4*>(ws + L.tpart);
   lp.logits = reinterpret_cast<float*>(ws + L.logits);
   lp.status = status;
+  // the draft rows' statistics come from the GEMM kernel's row warps (none
+  // when only the GEMM is timed)
+  lp.rows = rp;
+  if (a.gemm_only) lp.rows.draft = nullptr;
   const int lm_grid = L.n_tiles < dev.sms ? L.n_tiles : dev.sms;
-  if (a.gemm_only) {  // first kernel of the call: plain stream order
-    lmhead_kernel<<<lm_grid, kLmThreads, plan.smem, a.stream>>>(lp);
-    return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
-  }
-  if (launch_pdl(lmhead_kernel, dim3(lm_grid), dim3(kLmThreads), plan.smem, a.stream, lp) != cudaSuccess)
-    return SPEC_ERR_CUDA;
+  // first kernel of the call: plain stream order (the previous call's last
+  // kernel still reads this workspace)
+  lmhead_kernel<<<lm_grid, kLmThreads, plan.smem, a.stream>>>(lp);
+  if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
+  if (a.gemm_only) return SPEC_OK;
 
   // 3. decision, 4. residual / bonus masses and the draw
   LmTailParams tp = {};
