@@ -488,6 +488,131 @@ __device__ __forceinline__ void tk_sort_keys_desc(unsigned long long* a, int n, 
   __syncthreads();
 }
 
+constexpr int kTkWarpList = 128;  // lists finished by one warp (4 entries per lane)
+
+__device__ __forceinline__ int warp_min_i(int v) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, off));
+  return v;
+}
+
+// Rank sort of n <= kTkWarpList distinct keys by one warp, descending.
+__device__ __forceinline__ void tk_warp_sort_desc(unsigned long long* a, int n, unsigned long long* tmp) {
+  const int lane = threadIdx.x & 31;
+  for (int i = lane; i < n; i += 32) {
+    const unsigned long long x = a[i];
+    int r = 0;
+#pragma unroll 4
+    for (int j = 0; j < n; ++j) r += (a[j] > x) ? 1 : 0;
+    tmp[r] = x;
+  }
+  __syncwarp();
+  for (int i = lane; i < n; i += 32) a[i] = tmp[i];
+  __syncwarp();
+}
+
+// The select kernel's work after K's superset is in sk, for a list of at
+// most kTkWarpList entries, by one warp: the same steps and the same
+// arithmetic as the block-wide path (whose scans reduce to warp 0's when
+// every entry sits in warp 0), without block barriers.
+__device__ __noinline__ void tk_finish_warp(const TopkParams& p, int slot, int k, int count, bool greedy,
+                                            float temp, int dtok, unsigned long long* sk,
+                                            unsigned long long* tmp) {
+  const int lane = threadIdx.x & 31;
+  tk_warp_sort_desc(sk, count, tmp);  // logit descending, index ascending
+  {
+    // K: the entries whose key reaches the k-th largest; ties with it stay
+    const uint32_t kth = static_cast<uint32_t>(sk[min(k, count) - 1] >> 32);
+    int c = count;
+    for (int j = k + lane; j < count; j += 32)
+      if (static_cast<uint32_t>(sk[j] >> 32) < kth) c = min(c, j);
+    count = warp_min_i(c);
+  }
+  const int argmax = static_cast<int>(0xffffffffu - static_cast<uint32_t>(sk[0] & 0xffffffffull));
+  if (greedy) {
+    if (lane == 0) p.rowtk[slot] = make_float4(__int_as_float(0), kNegHuge, 0.f, __int_as_float(argmax));
+    return;
+  }
+  // ---- softmax over K, the top-p cut, the normaliser of K' ----
+  const float ks = kLog2e / temp;
+  const float mk = key_logit(static_cast<uint32_t>(sk[0] >> 32)) * ks;
+  float e[4];
+  uint32_t kj[4];
+  F2 my = f2_from(0.f);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {  // this lane's entries 4l .. 4l+3
+    const int j = 4 * lane + q;
+    kj[q] = (j < count) ? static_cast<uint32_t>(sk[j] >> 32) : 0u;
+    e[q] = (j < count) ? ex2(fmaf(key_logit(kj[q]), ks, -mk)) : 0.f;
+    my = f2_add(my, f2_from(e[q]));
+  }
+  const int jprev = 4 * lane - 1;
+  const uint32_t kprev = (jprev >= 0 && jprev < count) ? static_cast<uint32_t>(sk[jprev] >> 32) : 0xffffffffu;
+  const F2 incl = warp_scan_incl(my);
+  const F2 S = {__shfl_sync(0xffffffffu, incl.hi, 31), __shfl_sync(0xffffffffu, incl.lo, 31)};
+  int cut = count;
+  if (p.top_p < 1.f) {
+    const F2 thr = f2_mul_f(S, p.top_p);
+    F2 run = f2_sub(incl, my);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int j = 4 * lane + q;
+      if (j < count) {
+        const bool start = (j == 0) || (kj[q] != (q == 0 ? kprev : kj[q - 1]));
+        if (start && !f2_gt(thr, run)) cut = min(cut, j);
+        run = f2_add(run, f2_from(e[q]));
+      }
+    }
+    cut = warp_min_i(cut);
+  }
+  F2 my2 = f2_from(0.f);
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    if (4 * lane + q < cut) my2 = f2_add(my2, f2_from(e[q]));
+  const F2 incl2 = warp_scan_incl(my2);
+  const float lse2 = log2f(__shfl_sync(0xffffffffu, incl2.hi, 31) + __shfl_sync(0xffffffffu, incl2.lo, 31));
+  // ---- K' re-sorted by vocabulary index, written out ----
+  unsigned long long mine[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int j = 4 * lane + q;
+    mine[q] = 0ull;
+    if (j < cut) {
+      const uint32_t idx = 0xffffffffu - static_cast<uint32_t>(sk[j] & 0xffffffffull);
+      mine[q] = (static_cast<unsigned long long>(0xffffffffu - idx) << 32) | kj[q];
+    }
+  }
+  __syncwarp();
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    if (4 * lane + q < cut) sk[4 * lane + q] = mine[q];
+  __syncwarp();
+  tk_warp_sort_desc(sk, cut, tmp);  // index ascending
+  int* li = p.list_idx + static_cast<size_t>(slot) * kTkStore;
+  float* lv = p.list_val + static_cast<size_t>(slot) * kTkStore;
+  bool found = false;
+  float xd = 0.f;
+  for (int j = lane; j < cut; j += 32) {
+    const int idx = static_cast<int>(0xffffffffu - static_cast<uint32_t>(sk[j] >> 32));
+    const float x = key_logit(static_cast<uint32_t>(sk[j] & 0xffffffffull));
+    li[j] = idx;
+    lv[j] = x;
+    if (idx == dtok) {
+      found = true;
+      xd = x;
+    }
+  }
+  // the logit of the row's draft token if it was kept (indices are distinct:
+  // at most one lane finds it)
+  const unsigned fm = __ballot_sync(0xffffffffu, found);
+  if (fm == 0u) {
+    if (lane == 0) p.rowd[slot] = make_float2(0.f, 0.f);
+  } else if (lane == __ffs(fm) - 1) {
+    p.rowd[slot] = make_float2(xd, 1.f);
+  }
+  if (lane == 0) p.rowtk[slot] = make_float4(__int_as_float(cut), mk, lse2, __int_as_float(argmax));
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kTkThreads, 2) topk_select_kernel(const __grid_constant__ TopkParams p) {
   constexpr int P = Elt<T>::kPerVec;
@@ -563,6 +688,10 @@ __global__ void __launch_bounds__(kTkThreads, 2) topk_select_kernel(const __grid
   if (count > kTkStore) {  // more tied entries than the kept list holds
     if (threadIdx.x == 0) atomicOr(p.status, kStatusTopkOverflow);
     count = kTkStore;
+  }
+  if (count <= kTkWarpList) {  // block-uniform: a short list is finished by warp 0
+    if (threadIdx.x < 32) tk_finish_warp(p, slot, k, count, greedy, temp, dtok, sk, sort_tmp);
+    return;
   }
   tk_sort_keys_desc(sk, count, sort_tmp);  // logit descending, index ascending
   {
