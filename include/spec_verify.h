@@ -321,7 +321,9 @@ int spec_verify_lmhead_sample(const void *hidden, const void *W, const void *dra
 /*
  * Timing / profiling aid: the same arguments and checks as
  * spec_verify_lmhead_sample, but only its lm_head GEMM kernel is enqueued, in
- * the launch configuration that call uses.  Outputs are not written.
+ * the launch configuration that call uses, and without the draft rows' chunk
+ * statistics that kernel also computes in a whole call.  Outputs are not
+ * written.
  */
 int spec_verify_lmhead_gemm_only(const void *hidden, const void *W, const void *draft_logits,
                                  const int32_t *draft_tokens, const float *temperature,
