@@ -20,7 +20,7 @@ five source pages are:
 * [Self-spec]  "自投机解码：层跳过与拒绝采样实现大模型推理加速", §3.1 贪心解码,
                §3.2 采样解码, §3.3 随机数与 batch 内对齐, §4.1, §4.2.
 
-Readings where the pages are silent (each is listed in the design doc):
+Readings where the pages are silent:
 
 * accept iff ``u < rho`` with ``u`` in [0, 1); ``q(d) == 0`` accepts.
 * inverse CDF in ascending vocabulary order, strict ``>``: token
@@ -34,8 +34,7 @@ Readings where the pages are silent (each is listed in the design doc):
   logits, lowest index on ties; the greedy replacement / bonus is that argmax.
 
 Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
-(closed forms, exhaustive enumeration, brute force, library routines); see the
-pin table in the design doc.
+(closed forms, exhaustive enumeration, brute force, library routines).
 """
 from __future__ import annotations
 
@@ -132,9 +131,12 @@ def inverse_cdf(w: np.ndarray, u: float) -> tuple[int, float]:
     """Sample index k = min{k : C(k) > u * Z}, C the running sum of w, Z = C(V-1).
 
     Returns (k, margin) where margin is the distance in u units from u to the
-    nearer edge [C(k-1)/Z, C(k)/Z) of the chosen interval.  When rounding
-    leaves no index with C(k) > u*Z, the last index with w > 0 is taken and
-    the margin is 0.
+    nearer edge [C(k-1)/Z, C(k)/Z) of the chosen interval that another token
+    lies beyond.  The outer edges 0 and Z are not decision boundaries: below
+    the first token with weight nothing else can be drawn, and past the total
+    the last token with weight is drawn, so an edge with no weight beyond it
+    does not count.  When rounding leaves no index with C(k) > u*Z, the last
+    index with w > 0 is taken and the margin is 0.
     """
     c = np.cumsum(w)
     z = c[-1]
@@ -144,8 +146,9 @@ def inverse_cdf(w: np.ndarray, u: float) -> tuple[int, float]:
         nz = np.flatnonzero(w > 0)
         return int(nz[-1]), 0.0
     lo = c[k - 1] if k > 0 else 0.0
-    margin = min(u - lo / z, c[k] / z - u)
-    return k, float(margin)
+    below = u - lo / z if lo > 0.0 else math.inf      # a token with weight lies below
+    above = c[k] / z - u if c[k] < z else math.inf     # a token with weight lies above
+    return k, float(min(below, above))
 
 
 # ---------------------------------------------------------------------------
@@ -286,8 +289,10 @@ def truncate_probs(logits, temperature: float, top_k: int, top_p: float):
          top_p of pk (a tie group stays together; the most likely tokens are
          always kept);
     p  = softmax(l / T) over K', 0 elsewhere.
-    margin = min over x in K of |mass strictly above x - top_p|: how far the
-    top-p cut is from flipping (inf when top_p >= 1).
+    margin = min over x in K below the most likely tie group of
+    |mass strictly above x - top_p|: how far the top-p cut is from flipping
+    (inf when top_p >= 1).  The most likely group (mass above it 0) is kept
+    for every top_p > 0, so it sets no boundary.
     """
     l = _as_f64(logits)
     z = l / float(temperature)
@@ -305,7 +310,8 @@ def truncate_probs(logits, temperature: float, top_k: int, top_p: float):
     first = np.searchsorted(-lk, -lk, side="left")
     above = cum[first]
     keep = above < top_p
-    margin = math.inf if top_p >= 1.0 else float(np.min(np.abs(above - top_p)))
+    cuts = above[above > 0.0]
+    margin = math.inf if (top_p >= 1.0 or cuts.size == 0) else float(np.min(np.abs(cuts - top_p)))
     kept = idx_k[keep]
     p = np.zeros_like(l)
     zz = z[kept]

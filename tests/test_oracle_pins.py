@@ -930,3 +930,226 @@ def test_verify_sample_sparse_empty_rows_accept_every_draft():
     assert r.n == gamma and r.tokens[:gamma] == [5, 9, 60]
     p = scipy.special.softmax(target[0, gamma] / 0.9)
     assert r.tokens[gamma] == int(np.searchsorted(np.cumsum(p), 0.37, side="right"))
+
+
+# ---------------------------------------------------------------------------
+# the excusal margins.  A GPU result that differs from the oracle is excused
+# only where the oracle's margin is below the agreed window, so each margin is
+# pinned by what it promises, not by its formula: moving any one uniform (or
+# top_p) that took part in a decision by less than the margin leaves the
+# output unchanged, and moving one of them a little further than the margin,
+# towards the boundary it is nearest to, changes it.
+# ("Gemma 4 Multi-Token Prediction (MTP) 深度解析" §2.2: accept with
+# probability min(1, p/q); the stated 1e-6 window on uniforms near a boundary)
+# ---------------------------------------------------------------------------
+def _margin_cases(n, seed):
+    """Small random sequences: V in [3, 40], gamma in [1, 5], T in [0.4, 1.6],
+    draft logits = target + noise, drafts drawn from q."""
+    rng = np.random.default_rng(seed)
+    for _ in range(n):
+        V = int(rng.integers(3, 41))
+        g = int(rng.integers(1, 6))
+        T = float(rng.uniform(0.4, 1.6))
+        lt = rng.normal(0, 1.5, (g + 1, V))
+        ld = lt[:g] + rng.normal(0, float(rng.uniform(0.2, 1.5)), (g, V))
+        d = [int(rng.choice(V, p=scipy.special.softmax(ld[j] / T))) for j in range(g)]
+        yield lt, ld, d, T, rng.random(g), float(rng.random())
+
+
+def _same(a, b):
+    return a.n == b.n and a.tokens == b.tokens
+
+
+def margin_flip_violations(mod=so, n=400, seed=101):
+    """Cases where a SeqResult's margin breaks its promise (see above)."""
+    bad = 0
+    for lt, ld, d, T, ua, ur in _margin_cases(n, seed):
+        base = mod.verify_sample_seq(lt, ld, d, T, ua, ur)
+        m = base.margin
+        if not (0.0 < m < math.inf):
+            continue
+        # the uniforms that took part: u_accept[0..n] and u_resample
+        slots = [("a", j) for j in range(min(base.n + 1, len(d)))] + [("r", 0)]
+
+        def moved(slot, delta):
+            """The output with one uniform moved, or None when that takes the
+            resample uniform out of [0, 1), where the draw is not defined."""
+            a, r = list(ua), ur
+            if slot[0] == "a":
+                a[slot[1]] += delta     # u < rho is defined for any real u
+            else:
+                r += delta
+                if not 0.0 <= r < 1.0:
+                    return None
+            return mod.verify_sample_seq(lt, ld, d, T, a, r)
+
+        near = [moved(s, sgn * m * (1 - 1e-7)) for s in slots for sgn in (1, -1)]
+        far = [moved(s, sgn * (m * (1 + 1e-7) + 1e-15)) for s in slots for sgn in (1, -1)]
+        far = [r for r in far if r is not None]
+        inside = all(r is None or _same(base, r) for r in near)
+        beyond = not far or any(not _same(base, r) for r in far)
+        bad += (not inside) + (not beyond)
+    return bad
+
+
+def test_sample_margin_keeps_its_promise():
+    assert margin_flip_violations() == 0
+
+
+def test_acceptance_margin_hand_cases():
+    """rho = p(d)/q(d) = 0.5 exactly (dyadic rows): u sits 2^-20 from it."""
+    lt = np.log(np.array([[0.25, 0.75], [0.5, 0.5]]))
+    ld = np.log(np.array([[0.5, 0.5]]))
+    for u, accepted in ((0.5 - 2.0 ** -20, True), (0.5 + 2.0 ** -20, False)):
+        res = so.verify_sample_seq(lt, ld, [0], 1.0, [u], 0.3)   # draw edges 0.2 away or more
+        assert (res.n == 1) == accepted
+        assert abs(res.margin - 2.0 ** -20) < 1e-15      # the accept boundary is the nearer one
+    # a single token of residual weight: the draw has no boundary at all
+    res = so.verify_sample_seq(lt, ld, [0], 1.0, [0.9], 0.3)
+    assert res.n == 0 and res.tokens[0] == 1 and abs(res.margin - 0.4) < 1e-15
+    # far from rho the interior CDF edge of the draw is the nearer boundary:
+    # p = (1/8, 3/8, 1/2), q = (1/2, 1/4, 1/4), d = 0: rho = 1/4; after the
+    # rejection w = (0, 1/8, 1/4), edge 1/3 between tokens 1 and 2
+    lt3 = np.log(np.array([[0.125, 0.375, 0.5], [1 / 3, 1 / 3, 1 / 3]]))
+    ld3 = np.log(np.array([[0.5, 0.25, 0.25]]))
+    res = so.verify_sample_seq(lt3, ld3, [0], 1.0, [0.9], 0.3)
+    assert res.n == 0 and res.tokens[0] == 1 and abs(res.margin - (1 / 3 - 0.3)) < 1e-15
+    res = so.verify_sample_seq(lt3, ld3, [0], 1.0, [0.9], 0.34)
+    assert res.tokens[0] == 2 and abs(res.margin - (0.34 - 1 / 3)) < 1e-15
+    # rho >= 1 everywhere (q == p): the accept margins are rho - u = 1 - u
+    res = so.verify_sample_seq(lt, lt[:1], [1], 1.0, [0.9999], 0.3)
+    assert res.n == 1 and abs(res.margin - 1e-4) < 1e-12
+
+
+def test_greedy_margin_is_infinite():
+    lt = np.log(np.array([[0.25, 0.75], [0.5, 0.5]]))
+    assert so.verify_greedy_seq(lt, [1]).margin == math.inf
+
+
+def _kept(p):
+    return tuple(np.flatnonzero(p > 0))
+
+
+def topp_margin_violations(trunc=None, n=400, seed=103):
+    """Rows where truncate_probs's margin breaks its promise: moving top_p by
+    less than it keeps the kept set, moving it a little further (up or down)
+    changes it."""
+    trunc = trunc or so.truncate_probs
+    rng = np.random.default_rng(seed)
+    bad = 0
+    for _ in range(n):
+        V = int(rng.integers(2, 60))
+        l = rng.normal(0, float(rng.uniform(0.3, 3.0)), V)
+        T = float(rng.uniform(0.4, 1.6))
+        k = int(rng.integers(1, V + 3))
+        tp = float(rng.uniform(0.05, 0.99))
+        p, m = trunc(l, T, k, tp)
+        if not (0.0 < m < 1.0):
+            continue
+        base = _kept(p)
+        # top_p moves only inside its domain (0, 1]
+        near = [tp + s * m * (1 - 1e-7) for s in (1, -1)]
+        far = [tp + s * (m * (1 + 1e-7) + 1e-15) for s in (1, -1)]
+        inside = all(_kept(trunc(l, T, k, x)[0]) == base for x in near if 0.0 < x <= 1.0)
+        far = [x for x in far if 0.0 < x <= 1.0]
+        beyond = not far or any(_kept(trunc(l, T, k, x)[0]) != base for x in far)
+        bad += (not inside) + (not beyond)
+    return bad
+
+
+def test_topp_margin_keeps_its_promise():
+    assert topp_margin_violations() == 0
+
+
+def test_topp_margin_hand_case():
+    # masses (1/2, 1/4, 1/8, 1/8): the cuts sit at mass-above 0, 1/2, 3/4
+    l = np.log([0.5, 0.25, 0.125, 0.125])
+    for tp, m in ((0.6, 0.1), (0.74, 0.01), (0.3, 0.2), (0.95, 0.2), (0.1, 0.4)):
+        assert abs(so.truncate_probs(l, 1.0, 10, tp)[1] - m) < 1e-15
+
+
+def test_topkp_sequence_margin_covers_every_row():
+    """The sequence-level trunc_margin: moving top_p by less than it leaves the
+    whole verification unchanged."""
+    rng = np.random.default_rng(107)
+    for _ in range(60):
+        V, g = int(rng.integers(4, 30)), int(rng.integers(1, 4))
+        T = float(rng.uniform(0.5, 1.5))
+        lt = rng.normal(0, 1.5, (g + 1, V))
+        ld = lt[:g] + rng.normal(0, 0.7, (g, V))
+        k, tp = int(rng.integers(2, V + 1)), float(rng.uniform(0.3, 0.95))
+        d = [int(x) for x in rng.integers(0, V, g)]
+        ua, ur = rng.random(g), float(rng.random())
+        base = so.verify_sample_topkp_seq(lt, ld, d, T, k, tp, ua, ur)
+        m = base.trunc_margin
+        if not (0.0 < m < 1.0):
+            continue
+        for s in (1, -1):
+            r = so.verify_sample_topkp_seq(lt, ld, d, T, k, tp + s * m * (1 - 1e-7), ua, ur)
+            assert _same(base, r) and r.p_tok == base.p_tok and r.q_tok == base.q_tok
+        # a little beyond it, some row's kept set changes
+        rows = [lt[j] for j in range(g + 1)] + [ld[j] for j in range(g)]
+        assert any(_kept(so.truncate_probs(x, T, k, tp + s * (m * (1 + 1e-7) + 1e-15))[0]) !=
+                   _kept(so.truncate_probs(x, T, k, tp)[0]) for x in rows for s in (1, -1))
+
+
+def test_mutation_relative_acceptance_margin_is_caught(monkeypatch):
+    """|u - rho| / rho instead of |u - rho|."""
+    orig = so._decide_and_draw
+
+    def relative(P, Q, d, ua, ur, L_p, L_q):
+        r = orig(P, Q, d, ua, ur, L_p, L_q)
+        m = math.inf
+        for j in range(min(r.n + 1, len(d))):
+            rho = math.inf if r.q_tok[j] == 0 else r.p_tok[j] / r.q_tok[j]
+            if rho != math.inf:
+                m = min(m, abs(float(ua[j]) - rho) / rho)
+        w = so.residual_weights(P[r.n], Q[r.n]) if r.n < len(d) else P[len(d)]
+        r.margin = min(m, so.inverse_cdf(w, float(ur))[1])
+        return r
+    monkeypatch.setattr(so, "_decide_and_draw", relative)
+    assert margin_flip_violations(n=200) > 0
+
+
+def test_mutation_margin_of_the_wrong_decision_is_caught(monkeypatch):
+    """Only the deciding position's distance (j = n), not the accepted ones before it."""
+    orig = so._decide_and_draw
+
+    def last_only(P, Q, d, ua, ur, L_p, L_q):
+        r = orig(P, Q, d, ua, ur, L_p, L_q)
+        j = min(r.n, len(d) - 1)
+        rho = math.inf if r.q_tok[j] == 0 else r.p_tok[j] / r.q_tok[j]
+        m = abs(float(ua[j]) - rho) if rho != math.inf else math.inf
+        w = so.residual_weights(P[r.n], Q[r.n]) if r.n < len(d) else P[len(d)]
+        r.margin = min(m, so.inverse_cdf(w, float(ur))[1])
+        return r
+    monkeypatch.setattr(so, "_decide_and_draw", last_only)
+    assert margin_flip_violations(n=400) > 0
+
+
+def test_mutation_one_sided_cdf_margin_is_caught(monkeypatch):
+    """The distance to the upper CDF edge only."""
+    def upper_only(w, u):
+        c = np.cumsum(w)
+        z = c[-1]
+        k = int(np.searchsorted(c, u * z, side="right"))
+        if k >= len(w):
+            return int(np.flatnonzero(w > 0)[-1]), 0.0
+        return k, float(c[k] / z - u)
+    monkeypatch.setattr(so, "inverse_cdf", upper_only)
+    assert margin_flip_violations(n=200) > 0
+
+
+def test_mutation_topp_margin_below_the_cut_is_caught():
+    """The mass up to and including a token, instead of strictly above it."""
+    def below(logits, temperature, top_k, top_p):
+        p, _ = so.truncate_probs(logits, temperature, top_k, top_p)
+        l = np.asarray(logits, np.float64)
+        order = np.argsort(-l, kind="stable")
+        greater = np.searchsorted(-l[order], -l[order], side="left")
+        idx_k = order[greater < top_k]
+        zk = l[idx_k] / temperature
+        pk = scipy.special.softmax(zk)
+        upto = np.cumsum(pk)
+        return p, float(np.min(np.abs(upto - top_p)))
+    assert topp_margin_violations(trunc=below, n=200) > 0
