@@ -14,7 +14,7 @@ token logits (hidden . embedding) are computed only for the tokens of those
 clusters, about top_k * V / n_clusters of them.  Tokens outside get no logit:
 the draft distribution q is the softmax over the candidates and 0 elsewhere.
 
-Readings (listed in the design doc): the cluster score is the dot product with the
+Readings where the pages are silent: the cluster score is the dot product with the
 centroid (no bias, no scaling); the top_k are the largest scores with the
 lowest cluster index first among equal scores; candidates are reported in
 ascending token id.

@@ -64,6 +64,8 @@ def _compare(inp, top_k, top_p, out, num, dbg, seqs=None):
                     (b, j, dbg[b, j, :2], r.p_tok[j], r.q_tok[j])
                 for k, L in ((2, r.L_p[j]), (3, r.L_q[j])):
                     assert abs(dbg[b, j, k] - L) <= 1e-5 * max(1.0, abs(L)), (b, j, k, dbg[b, j, k], L)
+    # the same cap as the logit path: at most 1 % of a run (at least 2) excused
+    assert excused <= max(2, 0.01 * (exact + excused)), (exact, excused)
     return exact, excused
 
 

@@ -5,7 +5,7 @@ draft tokens and uniforms.  It contains none of the verify arithmetic and
 imports neither the oracle nor the CUDA library.
 
 Recipes (the pages name no dataset; these stand in for the workloads they
-describe, see DESIGN.md "Input recipe"):
+describe):
 
 * tiny      B=8,   gamma=4, V=4096,    fp32.  l_p ~ N(0, 2^2); l_q = l_p + N(0, 0.5^2).
 * single    B=1,   gamma=4, V=262144,  bf16.  Zipf-shaped target: -1.1*log(rank)
