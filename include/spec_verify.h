@@ -52,7 +52,9 @@ enum {
   SPEC_ERR_CUDA = -5,         /* a CUDA runtime call or kernel launch failed    */
   SPEC_ERR_TIMEOUT = -6,      /* device side: a bounded wait ran out            */
   SPEC_ERR_DEVICE_INPUT = -7, /* device side: a draft token outside [0, V)      */
-  SPEC_ERR_STATE = -8         /* host round driver: inconsistent bookkeeping   */
+  SPEC_ERR_STATE = -8,        /* host round driver: inconsistent bookkeeping   */
+  SPEC_ERR_DEVICE_BOUNDS = -9 /* device side, bounds-checked build only: an
+                                 index outside its extent (access skipped)    */
 };
 
 #define SPEC_MAX_GAMMA 31
@@ -273,13 +275,21 @@ int spec_verify_sample_reduce_only(const void *target_logits, const void *draft_
  * SPEC_ERR_WORKSPACE (B=128, gamma=8, V=262144 needs about 9 MB).
  *
  * - The first call on a device, with that device current, looks up the
- *   array's address and zeroes it (a synchronous cudaMemset); make that first
- *   call before any stream capture.  Nothing is ever allocated or freed.
+ *   array's address (cudaGetSymbolAddress; no memory is touched).  Every
+ *   call then clears the array's header and counters with cudaMemsetAsync on
+ *   the caller's stream, ahead of its kernel, so calls on any stream (a
+ *   non-blocking one included) start from a clean scratch.  Nothing is ever
+ *   allocated or freed.
  * - All calls share the one array: calls that overlap on the GPU (other
  *   streams, other host threads) race and give wrong tokens.  Serialise them.
- * - Device-side errors (a draft token outside [0, V), a wait that ran out)
- *   are recorded in the built-in scratch but cannot be read back through
- *   this entry point; host-side checks return codes as usual.
+ * - Device-side errors are recorded in the built-in scratch but cannot be
+ *   read back through this entry point; host-side checks return codes as
+ *   usual.  A draft token outside [0, V) is treated as rejected at its
+ *   position (greedy: replaced by the target argmax; sampling: the residual
+ *   draw runs there), so the outputs are well formed but meaningless for
+ *   that sequence; other sequences of the call are unaffected.  Callers that
+ *   cannot rule such tokens out should use spec_verify_sample and
+ *   spec_verify_status.
  */
 int spec_verify_sample_noalloc(const void *target_logits, const void *draft_logits,
                                spec_dtype dt, const int32_t *draft_tokens,

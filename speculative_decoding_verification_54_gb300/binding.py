@@ -23,6 +23,7 @@ SPEC_ERR_CUDA = -5
 SPEC_ERR_TIMEOUT = -6
 SPEC_ERR_DEVICE_INPUT = -7
 SPEC_ERR_STATE = -8
+SPEC_ERR_DEVICE_BOUNDS = -9
 MAX_GAMMA = 31
 
 EXPORTED = (

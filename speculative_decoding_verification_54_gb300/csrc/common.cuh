@@ -19,6 +19,23 @@ constexpr int kStatusTimeout = 1;
 constexpr int kStatusBadToken = 2;
 constexpr int kStatusTopkOverflow = 4;  // more tied entries than a truncation list holds
 constexpr int kStatusLimit = 8;         // more candidates than the caller's capacity (centroid head)
+constexpr int kStatusBounds = 16;       // an index failed its check (bounds-checked build only)
+
+// Bounds checks of the debug build.  Built with -DSPEC_CHECK_BOUNDS, every
+// checked index that falls outside its extent ORs kStatusBounds into the
+// status word and the access it guards is skipped (no trap: the context stays
+// usable and spec_verify_status reports it).  In the normal build the check
+// is the constant true and costs nothing.
+#ifdef SPEC_CHECK_BOUNDS
+constexpr bool kCheckBounds = true;
+__device__ __forceinline__ bool in_bounds(bool ok, int* status) {
+  if (!ok) atomicOr(status, kStatusBounds);
+  return ok;
+}
+#else
+constexpr bool kCheckBounds = false;
+__device__ __forceinline__ bool in_bounds(bool, int*) { return true; }
+#endif
 
 // wait limits in SM clock cycles (~2 GHz): about one second normally
 constexpr long long kWaitLimitCycles = 2000000000LL;
@@ -41,7 +58,9 @@ constexpr int kModeBonus = 2;     // all accepted: sample the bonus from p_gamma
 // ---------------------------------------------------------------------------
 struct WsHeader {
   int status;
-  int pad[63];
+  unsigned epoch;  // calls of the fused verify kernel completed on this workspace
+  int cta_done;    // CTAs of the running fused call that have finished
+  int pad[61];
 };
 
 struct RowStat {  // combined statistics of one logits row
@@ -57,6 +76,33 @@ struct SeqState {
   float ks;  // log2(e) / T
   int pad;
 };
+
+// 16-byte loads and stores of the per-row and per-sequence records through L2
+// (they are written and read by different CTAs of one launch)
+__device__ __forceinline__ RowStat ld_rowstat(const RowStat* a) {
+  const int4 v = __ldcg(reinterpret_cast<const int4*>(a));
+  RowStat r;
+  r.mk = __int_as_float(v.x);
+  r.argmax = v.y;
+  r.lse2 = __int_as_float(v.z);
+  r.pad = v.w;
+  return r;
+}
+__device__ __forceinline__ void st_rowstat(RowStat* a, const RowStat& r) {
+  __stcg(reinterpret_cast<int4*>(a), make_int4(__float_as_int(r.mk), r.argmax, __float_as_int(r.lse2), r.pad));
+}
+__device__ __forceinline__ SeqState ld_seqstate(const SeqState* a) {
+  const int4 v = __ldcg(reinterpret_cast<const int4*>(a));
+  SeqState s;
+  s.n = v.x;
+  s.mode = v.y;
+  s.ks = __int_as_float(v.z);
+  s.pad = v.w;
+  return s;
+}
+__device__ __forceinline__ void st_seqstate(SeqState* a, const SeqState& s) {
+  __stcg(reinterpret_cast<int4*>(a), make_int4(s.n, s.mode, __float_as_int(s.ks), s.pad));
+}
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) {
   return (x + a - 1) / a * a;

@@ -258,7 +258,9 @@ __device__ __forceinline__ void finish_item(const RowStatsParams& p, const Item&
                                             const uint4 (&v)[kVecPerLane], int lane) {
   const float4 r = (d.mode == kRowFull) ? reduce_full<T>(v, d.ks)
                                         : reduce_argmax<T>(v, d.chunk * p.CE, lane);
-  if (lane == 0) p.partials[static_cast<size_t>(d.slot) * p.cpr + d.chunk] = r;
+  if (lane == 0 && in_bounds(d.slot >= 0 && d.slot < p.B * (2 * p.gamma + 1) && d.chunk >= 0 && d.chunk < p.cpr,
+                             p.status))
+    p.partials[static_cast<size_t>(d.slot) * p.cpr + d.chunk] = r;
   if constexpr (kSubMax) {
     // block j of the chunk is vector slot j of every lane (32 consecutive
     // vectors).  A warp reduce-scatter: each exchange halves the values a

@@ -321,6 +321,7 @@ __device__ __forceinline__ void draw_token(const SampleParams& p, int b, const S
 
   // ---- level 2: which entry inside the chunk (block-wide) ----
   const int chunk = s_chunk;
+  if (!in_bounds(chunk >= 0 && chunk < p.cpr, p.dp.status)) return;
   const bool residual = s_resid;
   const F2 local = s_local;
   const int rowp = (s.mode == kModeResidual) ? s.n : g;  // the Z = 0 fallback keeps row n
@@ -406,6 +407,7 @@ __global__ void __launch_bounds__(kTailThreads, 2) tail_kernel(const __grid_cons
   __syncthreads();
   const SeqState s = s_seq;
   if (s.mode != kModeResidual && s.mode != kModeBonus) return;
+  if (!in_bounds(s.n >= 0 && s.n <= g, p.dp.status)) return;
 
   // ---- chunk masses of the row (pair) to draw from, this CTA's share ----
   const int per = (p.cpr + gridDim.x - 1) / gridDim.x;

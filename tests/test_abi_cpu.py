@@ -39,6 +39,17 @@ def test_library_exports_every_declared_symbol(lib):
     assert set(declared_functions()) <= set(sv.EXPORTED) | {"spec_verify_error_string"}
 
 
+def test_checked_build_exports_the_same_symbols():
+    """The bounds-checked debug build (-DSPEC_CHECK_BOUNDS) loads and exports
+    every declared entry point too."""
+    path = _build.build(checked=True)
+    chk = ctypes.CDLL(path)
+    for name in declared_functions():
+        assert hasattr(chk, name), name
+    chk.spec_verify_error_string.restype = ctypes.c_char_p
+    assert b"bounds" in chk.spec_verify_error_string(sv.SPEC_ERR_DEVICE_BOUNDS)
+
+
 def test_version_and_error_strings(lib):
     assert sv.spec_verify_version() >= 100
     assert sv.error_string(sv.SPEC_OK) == "ok"

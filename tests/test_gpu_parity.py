@@ -278,3 +278,46 @@ def test_bulk_copy_load_path_matches_direct_loads(sv, tmp_path):
         res[path] = dict(np.load(f))
     for k in res["ldg"]:
         assert np.array_equal(res["ldg"][k], res["tma"][k], equal_nan=True), k
+
+
+_CHAIN_CHILD = r"""
+import sys, numpy as np, torch
+sys.path.insert(0, sys.argv[1])
+import speculative_decoding_verification_54_gb300 as sv
+import workloads as wl
+import oracle
+from tests.gpu_util import to_device, run_sample, run_greedy, compare, assert_tally, Tally
+torch.cuda.set_device(0)
+t = Tally()
+for inp in (wl.make_round("tiny", 3), wl.make_round("batched", 7),
+            wl.make_custom(6, 4, 3 * 2048 + 24, dtype="bf16", profile="zipf",
+                           temperature=("alternate", 0.0, 0.9), seed=21)):
+    ws = sv.make_workspace(inp.B, inp.gamma, inp.V)
+    d = to_device(inp, torch.device("cuda:0"))
+    tok, num, dbg, st = run_sample(sv, d, ws)
+    assert st == 0
+    t.merge(compare(oracle.verify_sample(inp.target, inp.draft, inp.draft_tokens, inp.temperature,
+                                         inp.u_accept, inp.u_resample), tok, num, dbg))
+    gt, gn, st = run_greedy(sv, d, ws)
+    assert st == 0
+    for b, r in enumerate(oracle.verify_greedy(inp.target, inp.draft_tokens)):
+        assert int(gn[b]) == r.n and [int(x) for x in gt[b]] == r.tokens
+assert_tally(t)
+print("ok", t.checked, t.exact, t.excused)
+"""
+
+
+@pytest.mark.parametrize("chain", ["fused", "two"])
+def test_each_verify_chain_matches_the_oracle(sv, chain):
+    """Both verify paths, the single persistent kernel (SPECV_CHAIN=fused) and
+    the two-kernel chain of row reducer and tail kernel (SPECV_CHAIN=two),
+    pass the same parity checks in a fresh process."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, SPECV_CHAIN=chain)
+    r = subprocess.run([sys.executable, "-c", _CHAIN_CHILD, root], env=env, cwd=root,
+                       capture_output=True, text=True, timeout=900)
+    assert r.returncode == 0, r.stderr[-3000:]
+    assert r.stdout.startswith("ok")

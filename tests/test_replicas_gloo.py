@@ -84,15 +84,26 @@ def test_reference_arm_runs_on_rank_zero_only():
 
 
 def test_oracle_pool_on_all_cores_runs_every_task():
-    """The all-cores oracle leg of the bench's cpu_baseline: spawned workers
-    attach the round's logits (fp32 here, bf16 in the bench) from shared
-    memory and verify one sequence per task; every task completes and the
-    shared blocks are released."""
+    """The all-cores oracle leg of the bench's cpu_baseline and parity block:
+    spawned workers attach the round's logits (fp32 here, bf16 in the bench)
+    from shared memory the parent fills, verify one sequence per task and
+    report its acceptance rates; every task completes, the results equal the
+    oracle's own, and the shared blocks are released."""
     sys.path.insert(0, ROOT)
     import bench
     import workloads as wl
     inp = wl.make_round("tiny", 0)
     h = dict(target=inp.target, draft=inp.draft, draft_tokens=inp.draft_tokens, temperature=inp.temperature,
              u_accept=inp.u_accept, u_resample=inp.u_resample)
-    n, el = bench._oracle_all_cores(h, 6, 2)
-    assert n == 6 and el > 0
+    import oracle
+    with bench._oracle_rw_pool(h, 2) as (pool, arrs):
+        arrs[0][...] = h["target"]
+        arrs[1][...] = h["draft"]
+        tasks = [(b, h["draft_tokens"][b], float(h["temperature"][b]), h["u_accept"][b],
+                  float(h["u_resample"][b])) for b in range(inp.B)]
+        got = dict(pool.map(bench._oracle_rw_verify, tasks, chunksize=1))
+        alphas = dict(pool.map(bench._oracle_rw_alpha, [(b, float(h["temperature"][b])) for b in range(inp.B)]))
+    ref = oracle.verify_sample(inp.target, inp.draft, inp.draft_tokens, inp.temperature, inp.u_accept,
+                               inp.u_resample)
+    assert [got[b].tokens for b in range(inp.B)] == [r.tokens for r in ref]
+    assert all(len(alphas[b]) == inp.gamma and all(0.0 < a <= 1.0 for a in alphas[b]) for b in range(inp.B))
