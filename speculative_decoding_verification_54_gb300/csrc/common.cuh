@@ -58,9 +58,7 @@ constexpr int kModeBonus = 2;     // all accepted: sample the bonus from p_gamma
 // ---------------------------------------------------------------------------
 struct WsHeader {
   int status;
-  unsigned epoch;  // calls of the fused verify kernel completed on this workspace
-  int cta_done;    // CTAs of the running fused call that have finished
-  int pad[61];
+  int pad[63];
 };
 
 struct RowStat {  // combined statistics of one logits row

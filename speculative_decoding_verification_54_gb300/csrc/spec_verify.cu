@@ -23,7 +23,6 @@
 #include "centroid.cuh"
 #include "common.cuh"
 #include "decide.cuh"
-#include "fused.cuh"
 #include "lmhead.cuh"
 #include "lmtail.cuh"
 #include "rowstats.cuh"
@@ -48,14 +47,6 @@ struct DeviceInfo {
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
-// SPECV_CHAIN selects the verify path of spec_verify_sample / _greedy:
-// "fused" the single persistent kernel, "two" the two-kernel chain (row
-// reducer, then tail); the same results up to the 1e-6 boundary window.
-const bool g_two_kernel_chain = [] {
-  const char* e = std::getenv("SPECV_CHAIN");
-  return !(e != nullptr && std::strcmp(e, "fused") == 0);
-}();
-
 int device_info(DeviceInfo* out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SPEC_ERR_CUDA;
@@ -95,7 +86,7 @@ int device_info(DeviceInfo* out) {
 }
 
 struct Layout {
-  size_t header, partials, mass, tail_done, cand, rowstat, seq, row_cnt, sync, total;
+  size_t header, partials, mass, tail_done, cand, total;
 };
 
 // Offsets of the workspace regions for a call with (B, gamma, V); sized for
@@ -115,16 +106,6 @@ Layout layout(int B, int gamma, int V) {
   off += align_up(static_cast<size_t>(B) * kCounterStride * sizeof(int), 256);
   L.cand = off;  // per-candidate outputs of the multi-candidate entry: tokens [B, gamma+1], counts [B]
   off += align_up(static_cast<size_t>(B) * (gamma + 2) * sizeof(int32_t), 256);
-  // the fused verify kernel: combined rows, decisions and its counters (zero
-  // when no call is running; the claim words carry an epoch instead)
-  L.rowstat = off;
-  off += align_up(slots * sizeof(RowStat), 256);
-  L.seq = off;
-  off += align_up(static_cast<size_t>(B) * sizeof(SeqState), 256);
-  L.row_cnt = off;
-  off += align_up(slots * kRowCntStride * sizeof(int), 256);
-  L.sync = off;
-  off += align_up(static_cast<size_t>(B) * sizeof(SeqSync), 256);
   L.total = off;
   return L;
 }
@@ -269,69 +250,9 @@ int run_chain(const Common& a, bool sampling) {
   return SPEC_OK;
 }
 
-// The whole verify step in one persistent launch (fused.cuh).  Returns
-// SPEC_ERR_UNSUPPORTED when the work list would not fit 32-bit item indices
-// (the caller then runs the two-kernel chain).
-template <typename T>
-int run_fused(const Common& a, bool sampling) {
-  const Layout L = layout(a.B, a.gamma, a.V);
-  if (a.ws_bytes < L.total) return SPEC_ERR_WORKSPACE;
-  DeviceInfo dev;
-  if (device_info(&dev) != SPEC_OK) return SPEC_ERR_CUDA;
-  const Plan pl = make_plan(a.B, a.gamma, a.V, sizeof(T), dev.sms, sampling, kLdg);
-  const unsigned long long cpr = static_cast<unsigned long long>(pl.cpr);
-  const unsigned long long U1 = 2ull * a.gamma * cpr;
-  // residual items of sequence b follow `lag` phase-1 units (about 8 MB of
-  // streaming later, so its decision is usually published when they start)
-  const unsigned long long unit_bytes = U1 * static_cast<unsigned long long>(pl.CE) * sizeof(T);
-  unsigned long long lag = ((8ull << 20) + unit_bytes - 1) / unit_bytes;
-  if (lag < 1) lag = 1;
-  if (lag > static_cast<unsigned long long>(a.B)) lag = a.B;
-  const unsigned long long E1 = a.B * U1 + (a.B - lag) * cpr;
-  const unsigned long long N = E1 + a.B * cpr + lag * cpr;
-  if (N + 2ull * dev.sms * kFusedWarps >= (1ull << 31)) return SPEC_ERR_UNSUPPORTED;
-  uint8_t* ws = static_cast<uint8_t*>(a.ws);
-  FusedParams fp;
-  fp.target = a.target;
-  fp.draft = sampling ? a.draft : nullptr;
-  fp.draft_tokens = a.draft_tokens;
-  fp.temperature = sampling ? a.temperature : nullptr;
-  fp.u_accept = a.u_accept;
-  fp.u_resample = a.u_resample;
-  fp.out_tokens = a.out_tokens;
-  fp.out_num = a.out_num;
-  fp.out_debug = sampling ? a.out_debug : nullptr;
-  fp.partials = reinterpret_cast<float4*>(ws + L.partials);
-  fp.rowstat = reinterpret_cast<RowStat*>(ws + L.rowstat);
-  fp.seq = reinterpret_cast<SeqState*>(ws + L.seq);
-  fp.mass = reinterpret_cast<float*>(ws + L.mass);
-  fp.row_cnt = reinterpret_cast<int*>(ws + L.row_cnt);
-  fp.sync = reinterpret_cast<SeqSync*>(ws + L.sync);
-  fp.header = reinterpret_cast<WsHeader*>(ws + L.header);
-  fp.B = a.B;
-  fp.gamma = a.gamma;
-  fp.V = a.V;
-  fp.CE = pl.CE;
-  fp.cpr = pl.cpr;
-  fp.lag = static_cast<int>(lag);
-  fp.U1 = static_cast<unsigned>(U1);
-  fp.E1 = static_cast<unsigned>(E1);
-  fp.N = static_cast<unsigned>(N);
-  // two CTAs of 16 warps per SM, or fewer when the list is short
-  const unsigned long long want = (N + kFusedWarps - 1) / kFusedWarps;
-  const int grid = static_cast<int>(want < 2ull * dev.sms ? want : 2ull * dev.sms);
-  if (launch_pdl(verify_fused_kernel<T>, dim3(grid), dim3(kFusedThreads), 0, a.stream, fp) != cudaSuccess)
-    return SPEC_ERR_CUDA;
-  return SPEC_OK;
-}
-
 int dispatch(const Common& a, bool sampling) {
   if (a.dt != SPEC_F32 && a.dt != SPEC_BF16) return SPEC_ERR_UNSUPPORTED;
   const bool f32 = a.dt == SPEC_F32;
-  if (!a.debug && !a.reduce_only && !g_two_kernel_chain) {
-    const int e = f32 ? run_fused<float>(a, sampling) : run_fused<__nv_bfloat16>(a, sampling);
-    if (e != SPEC_ERR_UNSUPPORTED) return e;
-  }
   return f32 ? run_chain<float>(a, sampling) : run_chain<__nv_bfloat16>(a, sampling);
 }
 

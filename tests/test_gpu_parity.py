@@ -307,17 +307,14 @@ print("ok", t.checked, t.exact, t.excused)
 """
 
 
-@pytest.mark.parametrize("chain", ["fused", "two"])
-def test_each_verify_chain_matches_the_oracle(sv, chain):
-    """Both verify paths, the single persistent kernel (SPECV_CHAIN=fused) and
-    the two-kernel chain of row reducer and tail kernel (SPECV_CHAIN=two),
-    pass the same parity checks in a fresh process."""
+def test_verify_chain_matches_the_oracle_in_a_fresh_process(sv):
+    """The verify chain (row reducer, then tail) passes the parity checks in a
+    fresh process on the tiny, batched and mixed greedy/sampled cases."""
     import os
     import subprocess
     import sys
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-    env = dict(os.environ, SPECV_CHAIN=chain)
-    r = subprocess.run([sys.executable, "-c", _CHAIN_CHILD, root], env=env, cwd=root,
+    r = subprocess.run([sys.executable, "-c", _CHAIN_CHILD, root], cwd=root,
                        capture_output=True, text=True, timeout=900)
     assert r.returncode == 0, r.stderr[-3000:]
     assert r.stdout.startswith("ok")
