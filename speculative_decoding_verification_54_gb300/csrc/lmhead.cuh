@@ -4,8 +4,9 @@
 // the verify positions times the tied embedding ("Gemma 4 Multi-Token
 // Prediction (MTP) 深度解析" §3.1: lm_head shares embed_tokens; "Gemma 4 -
 // Drafter 解析", 高效 Embedder: the LM head multiplies the hidden state by the
-// embedding table).  They are never written to memory: the epilogue turns each
-// 128-entry vocabulary tile straight into the statistics the verify step needs.
+// embedding table).  No row is read back to be reduced: the epilogue turns
+// each 128-entry vocabulary tile straight into the statistics the verify step
+// needs.
 //
 // Orientation: A = a 128-row tile of W (vocabulary entries: the MMA's M and
 // the TMEM lanes), B = the hidden rows (the MMA's N: up to 256 per MMA, so 320
@@ -33,8 +34,9 @@
 // rows that can be rejected (positions j < gamma of sampling sequences) are
 // also stored in fp32, a warp writing 32 consecutive vocabulary entries of a
 // row at once: the residual max(0, p_j - q_j) needs p_j's normaliser, known
-// only once the whole row is reduced, and storing these rows costs a third of
-// reading W a second time.
+// only once the whole row is reduced.  At B=64, gamma=4, H=1536 the store
+// measured 51 us of a 298 us launch, where recomputing the rows the draw
+// needs (a second pass over W for 64 rows) measured 175 us.
 #pragma once
 
 #include <cfloat>
