@@ -69,6 +69,21 @@ def test_head_exact_small(sv):
             assert np.array_equal(lg[r, :cnt[r]].astype(np.float64), l_ref)  # exact recipe: bitwise
 
 
+def test_head_exact_past_the_bitmap_vocabulary(sv):
+    """Above 262,144 tokens the candidates are ordered by the sort kernel (a
+    bitonic sort) instead of the selection kernel's ranks; same bar: bitwise."""
+    m = wl.make_centroid_model(V=262144 + 4096, H=256, n_clusters=64, seed=8, exact_sums=True, mu_sd=0.12,
+                               eps_sd=0.005)
+    rd = wl.make_centroid_round(m, B=2, gamma=1, exact_sums=True, draft_sd=0.05)
+    tok, lg, cnt, st = _run_head(sv, m, rd["hidden_draft"], 1)  # one cluster: about 4,160 candidates
+    assert st == sv.SPEC_OK
+    ref = oracle.centroid_head(rd["hidden_draft"], m.centroids, m.W_ord, m.cluster_off, m.ord2tok, 1)
+    for r, (t_ref, l_ref) in enumerate(ref):
+        assert cnt[r] == len(t_ref)
+        assert np.array_equal(tok[r, :cnt[r]], t_ref)
+        assert np.array_equal(lg[r, :cnt[r]].astype(np.float64), l_ref)
+
+
 def test_head_all_clusters_is_every_token(sv):
     m = wl.make_centroid_model(V=4096, H=512, n_clusters=64, seed=5, exact_sums=True)
     rd = wl.make_centroid_round(m, B=2, gamma=2, exact_sums=True)
