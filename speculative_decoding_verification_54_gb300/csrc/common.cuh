@@ -75,33 +75,6 @@ struct SeqState {
   int pad;
 };
 
-// 16-byte loads and stores of the per-row and per-sequence records through L2
-// (they are written and read by different CTAs of one launch)
-__device__ __forceinline__ RowStat ld_rowstat(const RowStat* a) {
-  const int4 v = __ldcg(reinterpret_cast<const int4*>(a));
-  RowStat r;
-  r.mk = __int_as_float(v.x);
-  r.argmax = v.y;
-  r.lse2 = __int_as_float(v.z);
-  r.pad = v.w;
-  return r;
-}
-__device__ __forceinline__ void st_rowstat(RowStat* a, const RowStat& r) {
-  __stcg(reinterpret_cast<int4*>(a), make_int4(__float_as_int(r.mk), r.argmax, __float_as_int(r.lse2), r.pad));
-}
-__device__ __forceinline__ SeqState ld_seqstate(const SeqState* a) {
-  const int4 v = __ldcg(reinterpret_cast<const int4*>(a));
-  SeqState s;
-  s.n = v.x;
-  s.mode = v.y;
-  s.ks = __int_as_float(v.z);
-  s.pad = v.w;
-  return s;
-}
-__device__ __forceinline__ void st_seqstate(SeqState* a, const SeqState& s) {
-  __stcg(reinterpret_cast<int4*>(a), make_int4(s.n, s.mode, __float_as_int(s.ks), s.pad));
-}
-
 __host__ __device__ inline size_t align_up(size_t x, size_t a) {
   return (x + a - 1) / a * a;
 }

@@ -1146,9 +1146,9 @@ extern "C" int spec_verify_sample_noalloc(const void* target_logits, const void*
   if (L.total > kNoAllocScratchBytes) return SPEC_ERR_WORKSPACE;  // beyond the built-in scratch
   void* scratch = nullptr;
   if (int e = noalloc_scratch(&scratch)) return e;
-  // the header (status word, epoch) and the counters and claim words must
-  // start at zero; everything else in the scratch is written before it is
-  // read.  Both clears go on the caller's stream, ahead of the kernel.
+  // the header (status word) and the per-sequence counters must start at
+  // zero; everything else in the scratch is written before it is read.  Both
+  // clears go on the caller's stream, ahead of the kernels.
   unsigned char* sc = static_cast<unsigned char*>(scratch);
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(sc + L.header, 0, L.partials - L.header, st) != cudaSuccess ||
