@@ -569,8 +569,10 @@ int run_lm_chain(const LmArgs& a) {
   dp.V = a.V;
   if (launch_pdl(lm_decide_kernel, dim3(a.B), dim3(kLmTailThreads), 0, a.stream, tp) != cudaSuccess)
     return SPEC_ERR_CUDA;
-  // parts per sequence: about three CTAs per SM over the batch, >= 8 tiles each
-  int parts = (3 * dev.sms + a.B - 1) / a.B;
+  // parts per sequence: three CTAs per SM (76 registers x 256 threads) over the
+  // batch, rounded down so every CTA is resident in one wave, >= 8 tiles each
+  // (rounding up left a second wave of 56 CTAs at B=64: 1.4 us per round)
+  int parts = (3 * dev.sms) / a.B;
   if (parts > L.n_tiles / 8) parts = L.n_tiles / 8;
   if (parts > 64) parts = 64;
   if (parts < 1) parts = 1;
