@@ -214,23 +214,33 @@ def _check_envelope(res, b, inp, tok, num, dbg, eps_rows):
 
 
 def test_lmhead_realistic_recipe_full_size_within_envelope(sv, dev):
+    """Every sequence of one full-size round on the workload's own recipe.
+    Probabilities must meet the 1e-5 bar outright; a decision or token that
+    differs from the oracle's must lie inside the fp32-accumulation envelope
+    (_check_envelope), and such cases may be at most 1 % of the sequences."""
     B, gamma, V, H = 64, 4, 262144, 1536
     W = wl.make_lmhead_W(V, H, seed=0)
     inp = wl.make_lmhead_round(0, B=B, gamma=gamma, V=V, H=H, W_bits=W)
     ws = sv.make_workspace(B, gamma, V, H)
     tok, num, dbg, st = run_lm(sv, to_device_lm(inp, dev), ws)
     assert st == sv.SPEC_OK
-    seqs = [1, 12, 23, 34, 45, 56]
+    seqs = list(range(B))
     ref = _oracle(inp, seqs)
     hid = oracle.spec_oracle._as_f64(inp.hidden)
     Wf = oracle.spec_oracle._as_f64(W)
     kinds = []
+    max_dp = 0.0
     for res, b in zip(ref, seqs):
-        eps = _logit_error_bound(hid, Wf, list(range(b * (gamma + 1), (b + 1) * (gamma + 1))))
-        kinds.append(_check_envelope(res, b, inp, tok, num, dbg, eps))
-        # probabilities of the draft tokens: within the envelope too
+        same = int(num[b]) == res.n and [int(x) for x in tok[b]] == res.tokens
+        if same:
+            kinds.append("exact")
+        else:
+            eps = _logit_error_bound(hid, Wf, list(range(b * (gamma + 1), (b + 1) * (gamma + 1))))
+            kinds.append(_check_envelope(res, b, inp, tok, num, dbg, eps))
         for j in range(gamma):
-            kk = 2 * float(eps.max()) / float(inp.temperature[b])
-            assert abs(dbg[b, j, 0] - res.p_tok[j]) <= res.p_tok[j] * math.expm1(kk) + 1e-5
-            assert abs(dbg[b, j, 1] - res.q_tok[j]) <= 1e-5
-    print("realistic lm_head recipe:", kinds)
+            max_dp = max(max_dp, abs(dbg[b, j, 0] - res.p_tok[j]), abs(dbg[b, j, 1] - res.q_tok[j]))
+    assert max_dp <= 1e-5, max_dp
+    off = sum(k != "exact" for k in kinds)
+    assert off <= max(1, 0.01 * B), kinds
+    print(f"realistic lm_head recipe, one round: {kinds.count('exact')} exact of {B}, "
+          f"{off} inside the rounding envelope; max |dp| {max_dp:.2e}")
