@@ -152,24 +152,31 @@ struct LmEpiScratch {
 };
 
 // One accumulator chunk (nc hidden rows x 128 vocabulary entries) of tile
-// `tile`, by one group of four warps (this warp: lane quadrant `quad`).
+// `tile`: this group of four warps (this warp: lane quadrant `quad`) takes
+// the chunk's 32-row groups g0, g0 + 2, ... (the other group the rest), so
+// both groups work on a chunk at once and its TMEM slot is freed sooner.
 // Phase 1: per 32-row group, the warp's column maxima (and argmax where a row
 // is greedy) into red/redI.  Phase 2: lane l combines the four quadrants for
 // row l of each group.  Phase 3: exponentials against the row maxima, the
-// stored logits, and the warp's column sums into red; the TMEM chunk is free
-// after this phase.  Phase 4: the row partials.  The group loops stay rolled
-// (the unrolled bodies overflow the instruction cache); what crosses phases
-// lives in shared memory.
+// stored logits, and the warp's column sums into red; this group's reads of
+// the TMEM chunk end with this phase.  Phase 4: the row partials.  The group
+// loops stay rolled (the unrolled bodies overflow the instruction cache);
+// what crosses phases lives in shared memory.
 __device__ __forceinline__ void lm_epilogue_chunk(const LmParams& p, const LmRowTables& T, const LmEpiScratch& S,
-                                                  uint32_t tacc, int tile, int c, int quad, int lane, int bar_id,
-                                                  uint64_t* slot_empty) {
+                                                  uint32_t tacc, int tile, int c, int g0, int quad, int lane,
+                                                  int bar_id, uint64_t* slot_empty) {
   const int nc = p.nc, ng = nc / 32;
   const int x = tile * kLmTileV + quad * 32 + lane;  // this lane's vocabulary entry
   const bool xv = x < p.V;
+  // this group's row of phases 2 and 4: quadrant warp q takes the group's
+  // q-th 32-row group (at most (ng + 1) / 2 <= 4 of them)
+  const int my_g = g0 + 2 * quad;
+  const int col = my_g * 32 + lane;
+  const bool has_col = my_g < ng;
 
   // ---- phase 1 ----
 #pragma unroll 1
-  for (int g = 0; g < ng; ++g) {
+  for (int g = g0; g < ng; g += 2) {
     float v[32];
     int id[32];
     tmem_ld32(tacc + g * 32, v);
@@ -190,9 +197,8 @@ __device__ __forceinline__ void lm_epilogue_chunk(const LmParams& p, const LmRow
   }
   named_bar(bar_id, 128);
 
-  // ---- phase 2: the four quadrants of each row; the group's 128 threads
-  // take the chunk's rows in turn ----
-  for (int col = quad * 32 + lane; col < nc; col += 128) {
+  // ---- phase 2: the four quadrants of each of the group's rows ----
+  if (has_col) {
     const int row = c * nc + col;
     const bool rv = row < p.R;
     const bool gr = rv && T.greedy[row];
@@ -221,7 +227,7 @@ __device__ __forceinline__ void lm_epilogue_chunk(const LmParams& p, const LmRow
 
   // ---- phase 3 ----
 #pragma unroll 1
-  for (int g = 0; g < ng; ++g) {
+  for (int g = g0; g < ng; g += 2) {
     float v[32];
     tmem_ld32(tacc + g * 32, v);
     const int rb = c * nc + g * 32;
@@ -266,7 +272,7 @@ __device__ __forceinline__ void lm_epilogue_chunk(const LmParams& p, const LmRow
 
   // ---- phase 4 ----
   if (tile < p.n_tiles) {
-    for (int col = quad * 32 + lane; col < nc; col += 128) {
+    if (has_col) {
       const int row = c * nc + col;
       if (row < p.R) {
         const float2 f = S.fin[col];
@@ -306,7 +312,7 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_kernel(const __grid_cons
     }
     for (int s = 0; s < p.n_slots; ++s) {
       mbar_init(&sfull[s], 1);
-      mbar_init(&sempty[s], 4);
+      mbar_init(&sempty[s], 4 * kLmEpiGroups);  // every epilogue warp reads every chunk
     }
     for (int g = 0; g < kLmEpiGroups; ++g) s_abort[g] = 0;
     fence_mbar_init();
@@ -471,7 +477,7 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_kernel(const __grid_cons
     S.finI = reinterpret_cast<int*>(sc + 44 * p.nc);
     S.tb = reinterpret_cast<float*>(scratch + kLmEpiGroups * lm_scratch_bytes(p.nc) + e * kLmTransBytes);
     const int units = my_tiles * p.n_chunks;
-    for (int u = grp; u < units; u += kLmEpiGroups) {
+    for (int u = 0; u < units; ++u) {
       const int slot = u % p.n_slots;
       const bool got = __all_sync(0xffffffffu, mbar_wait(&sfull[slot], (u / p.n_slots) & 1, p.status,
                                                          kWaitLimitCycles));
@@ -482,7 +488,9 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_kernel(const __grid_cons
       const int t = u / p.n_chunks, c = u % p.n_chunks;
       const int tile = static_cast<int>(blockIdx.x) + t * static_cast<int>(gridDim.x);
       const uint32_t tacc = tmem + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(slot * p.nc);
-      lm_epilogue_chunk(p, T, S, tacc, tile, c, quad, lane, 1 + grp, &sempty[slot]);
+      // the groups alternate which takes the chunk's even 32-row groups, so
+      // over a tile of two chunks each takes the same number
+      lm_epilogue_chunk(p, T, S, tacc, tile, c, (grp + c) & 1, quad, lane, 1 + grp, &sempty[slot]);
     }
   } else {
     // ---------------- row warps: the draft rows' chunk statistics ----------------
