@@ -64,11 +64,13 @@ int device_info(DeviceInfo* out) {
     int optin = 0;
     cudaFuncAttributes fa;
     if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
-        cudaFuncGetAttributes(&fa, lmhead_kernel) != cudaSuccess)
+        cudaFuncGetAttributes(&fa, lmhead_kernel<2>) != cudaSuccess)
       return SPEC_ERR_CUDA;
     d.lm_max_dyn = optin - static_cast<int>(fa.sharedSizeBytes);
-    if (cudaFuncSetAttribute(lmhead_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, d.lm_max_dyn) !=
-        cudaSuccess)
+    if (cudaFuncSetAttribute(lmhead_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, d.lm_max_dyn) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(lmhead_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, d.lm_max_dyn) !=
+            cudaSuccess)
       return SPEC_ERR_CUDA;
     // the centroid head: cluster keys (4 B each) and the candidate ranking
     // (candidates plus the token bitmap and its prefix) in shared memory
@@ -531,7 +533,10 @@ int run_lm_chain(const LmArgs& a) {
   const int lm_grid = L.n_tiles < dev.sms ? L.n_tiles : dev.sms;
   // first kernel of the call: plain stream order (the previous call's last
   // kernel still reads this workspace)
-  lmhead_kernel<<<lm_grid, kLmThreads, plan.smem, a.stream>>>(lp);
+  if (plan.n_chunks == 1)
+    lmhead_kernel<1><<<lm_grid, kLmThreads, plan.smem, a.stream>>>(lp);
+  else
+    lmhead_kernel<2><<<lm_grid, kLmThreads, plan.smem, a.stream>>>(lp);
   if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
   if (a.gemm_only) return SPEC_OK;
 
