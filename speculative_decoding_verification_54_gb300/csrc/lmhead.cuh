@@ -78,15 +78,15 @@ struct LmParams {
   RowStatsParams rows;
 };
 
-// Dynamic shared memory: W ring, hidden ring, per epilogue group the
-// cross-warp scratch (red [4][nc] f32, redI [4][nc] i32, fin [nc] float2,
-// finM [nc] f32, finI [nc] i32), then per epilogue warp a transpose buffer
-// for the stored logits.
+// Dynamic shared memory: W ring, hidden ring, the epilogue's cross-warp
+// scratch (red [4][nc] f32, redI [4][nc] i32, fin [nc] float2, finM [nc] f32,
+// finI [nc] i32; the groups use disjoint rows of it), then per epilogue warp a
+// transpose buffer for the stored logits.
 __host__ __device__ inline uint32_t lm_scratch_bytes(int nc) { return static_cast<uint32_t>(nc) * 4u * 12u; }
 constexpr uint32_t kLmTransBytes = 8 * 32 * 4;  // per epilogue warp: 8 rows x 32 entries
 __host__ __device__ inline uint32_t lm_smem_bytes(int w_stages, int h_stages, uint32_t h_bytes, int nc) {
   return static_cast<uint32_t>(w_stages) * kLmWBytes + static_cast<uint32_t>(h_stages) * h_bytes +
-         kLmEpiGroups * lm_scratch_bytes(nc) + 4u * kLmEpiGroups * kLmTransBytes + 1024u;
+         lm_scratch_bytes(nc) + 4u * kLmEpiGroups * kLmTransBytes + 1024u;
 }
 
 __device__ __forceinline__ void named_bar(int id, int nthreads) {
@@ -475,13 +475,15 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_kernel(const __grid_cons
     // ---------------- epilogue: warps 3..10, two groups of four ----------------
     const int e = warp - 3, grp = e >> 2, quad = warp & 3;
     LmEpiScratch S;
-    uint8_t* sc = scratch + grp * lm_scratch_bytes(p.nc);
+    // one scratch for both groups: group g always takes the 32-row groups of
+    // parity g, so the two never touch the same rows of it
+    uint8_t* sc = scratch;
     S.red = reinterpret_cast<float*>(sc);
     S.redI = reinterpret_cast<int*>(sc + 16 * p.nc);
     S.fin = reinterpret_cast<float2*>(sc + 32 * p.nc);
     S.finM = reinterpret_cast<float*>(sc + 40 * p.nc);
     S.finI = reinterpret_cast<int*>(sc + 44 * p.nc);
-    S.tb = reinterpret_cast<float*>(scratch + kLmEpiGroups * lm_scratch_bytes(p.nc) + e * kLmTransBytes);
+    S.tb = reinterpret_cast<float*>(scratch + lm_scratch_bytes(p.nc) + e * kLmTransBytes);
     const int units = my_tiles * kChunks;
     for (int u = 0; u < units; ++u) {
       const int slot = u % p.n_slots;
@@ -494,9 +496,7 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_kernel(const __grid_cons
       const int t = u / kChunks, c = u % kChunks;
       const int tile = static_cast<int>(blockIdx.x) + t * static_cast<int>(gridDim.x);
       const uint32_t tacc = tmem + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(slot * p.nc);
-      // the groups alternate which takes the chunk's even 32-row groups, so
-      // over a tile of two chunks each takes the same number
-      lm_epilogue_chunk(p, T, S, tacc, tile, c, (grp + c) & 1, quad, lane, 1 + grp, &sempty[slot]);
+      lm_epilogue_chunk(p, T, S, tacc, tile, c, grp, quad, lane, 1 + grp, &sempty[slot]);
     }
   } else {
     // ---------------- row warps: the draft rows' chunk statistics ----------------
