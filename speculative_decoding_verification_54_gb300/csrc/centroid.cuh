@@ -269,9 +269,26 @@ __global__ void __launch_bounds__(kHeadThreads, 1) cand_sort_kernel(const __grid
     int* wpre = reinterpret_cast<int*>(bits + kHeadBitmapV / 32);
     const int nw = (p.V + 31) / 32;
     for (int i = t; i < nw; i += kHeadThreads) bits[i] = 0u;
-    for (int i = t; i < n; i += kHeadThreads) {
-      st_tok[i] = otok[i];
-      st_log[i] = olog[i];
+    // the candidates into shared memory, all of a thread's loads issued
+    // before its stores (n <= kHeadMaxCand = 16 per thread)
+    {
+      constexpr int kPer = kHeadMaxCand / kHeadThreads;
+      int32_t tk[kPer];
+      float lg[kPer];
+#pragma unroll
+      for (int j = 0; j < kPer; ++j) {
+        const int i = t + j * kHeadThreads;
+        tk[j] = (i < n) ? __ldcg(otok + i) : 0;
+        lg[j] = (i < n) ? __ldcg(olog + i) : 0.f;
+      }
+#pragma unroll
+      for (int j = 0; j < kPer; ++j) {
+        const int i = t + j * kHeadThreads;
+        if (i < n) {
+          st_tok[i] = tk[j];
+          st_log[i] = lg[j];
+        }
+      }
     }
     __syncthreads();
     for (int i = t; i < n; i += kHeadThreads) {
