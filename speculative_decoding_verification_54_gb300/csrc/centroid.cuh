@@ -9,10 +9,14 @@
 // against the drafter's hidden state, the top_k clusters are kept, and token
 // logits are computed only for their tokens.  Four kernels, chained with
 // programmatic dependent launch:
-//   cluster_score_kernel   z[r, c] = h[r] . C[c]  (fp32 sums of bf16 products;
-//                          each warp holds one centroid, the CTA stages
+//   cluster_score_*        z[r, c] = h[r] . C[c]  (fp32 sums of bf16 products):
+//                          for more than 16 hidden rows a tcgen05 GEMM (128
+//                          centroids x up to 256 hidden rows per CTA, K split
+//                          over up to 8 CTAs); for fewer, CUDA cores (each
+//                          warp holds one centroid, the CTA stages
 //                          kHeadRowBlock hidden rows in shared memory)
-//   cluster_topk_kernel    one CTA per row: radix select of the top_k scores
+//   cluster_topk_kernel    one CTA per row: adds the K-split partial scores in
+//                          order, radix select of the top_k scores
 //                          (the lowest index first among equal scores) and
 //                          the selected clusters' candidate offsets
 //   cand_logit_kernel      grid (top_k, R): one CTA per selected cluster, one
@@ -27,13 +31,15 @@
 #include <cuda_bf16.h>
 
 #include "common.cuh"
+#include "tc.cuh"
 #include "topkp.cuh"
 
 namespace specv {
 
 constexpr int kHeadThreads = 512;  // tk_sort_desc assumes 512-thread CTAs
 constexpr int kHeadWarps = kHeadThreads / 32;
-constexpr int kHeadRowBlock = 4;       // hidden rows staged per pass of cluster_score_kernel (32 KB)
+constexpr int kHeadRowBlock = 4;       // hidden rows staged per pass of cluster_score_cc_kernel (32 KB)
+constexpr int kHeadScoreTcRows = 16;   // more hidden rows than this: the scores on the tensor cores
 constexpr int kHeadMaxVecs = 8;        // 16-byte vectors per lane of one embedding row: H <= 2048
 constexpr int kHeadMaxClusters = 8192;  // cluster keys held in shared memory by cluster_topk_kernel
 constexpr int kHeadMaxTopK = 256;
@@ -46,7 +52,7 @@ struct HeadParams {
   const __nv_bfloat16* W_ord;      // [V, H], cluster by cluster
   const int32_t* cluster_off;      // [n_clusters + 1]
   const int32_t* ord2tok;          // [V]
-  float* scores;                   // [R, n_clusters] (workspace)
+  float* scores;                   // [ksplit, R, n_clusters] partial scores (workspace)
   int32_t* sel;                    // [R, top_k] selected clusters (workspace)
   int32_t* pos;                    // [R, top_k + 1] candidate offsets (workspace)
   int32_t* out_tok;                // [R, max_cand]
@@ -54,6 +60,7 @@ struct HeadParams {
   int32_t* out_count;              // [R]
   int* status;
   int R, H, V, n_clusters, top_k, max_cand;
+  int ksplit;                      // K parts of the score GEMM (partials to add)
 };
 
 // Dot product of one embedding row (held by the lanes: vector lane + 32k of
@@ -90,8 +97,12 @@ __device__ __forceinline__ void load_row_vecs(const __nv_bfloat16* row, int nv, 
     if (k < nv) e[k] = __ldg(v + lane + 32 * k);
 }
 
-// ---- 1. cluster scores: grid ceil(n_clusters / kHeadWarps) x row blocks ----
-__global__ void __launch_bounds__(kHeadThreads, 1) cluster_score_kernel(const __grid_constant__ HeadParams p) {
+// ---- 1a. cluster scores for few hidden rows, on the CUDA cores: grid
+// ceil(n_clusters / kHeadWarps) x row blocks; each warp holds one centroid,
+// the CTA stages kHeadRowBlock hidden rows in shared memory.  Up to 16 rows
+// this measured faster than the tensor-core GEMM below (R = 4: 37.6 against
+// 40.5 us per head call), whose split-K partials the selection must add ----
+__global__ void __launch_bounds__(kHeadThreads, 1) cluster_score_cc_kernel(const __grid_constant__ HeadParams p) {
   __shared__ __align__(16) __nv_bfloat16 hs[kHeadRowBlock * kHeadMaxVecs * 32 * 8];
   grid_dep_launch();
   grid_dep_wait();
@@ -115,6 +126,115 @@ __global__ void __launch_bounds__(kHeadThreads, 1) cluster_score_kernel(const __
     const float z = dot_row_smem(e, nv, dst + r * kHeadMaxVecs * 32);
     if (lane == 0) p.scores[static_cast<size_t>(r0 + r) * p.n_clusters + c] = z;
   }
+}
+
+// ---- 1b. cluster scores on the tensor cores (more than 16 hidden rows) ----
+// z[r, c] = h[r] . C[c] is a GEMM: A = 128 centroids (the MMA's M, the TMEM
+// lanes), B = a chunk of N hidden rows (the MMA's N), K = H in stages of 64
+// (128-byte swizzled rows) through a TMA ring.  Grid (tiles * ksplit, row
+// chunks): CTA (tile, part) takes the K steps [part*kper, (part+1)*kper) and
+// writes its partial sums to scores[part][r][c]; cluster_topk_kernel adds the
+// parts in order.  Warp 0 lane 0 loads, warp 1 lane 0 issues the MMAs, then
+// all four warps read the accumulator (warp w: TMEM lanes 32w..32w+31).
+constexpr int kScThreads = 128;
+constexpr int kScStages = 4;
+constexpr int kScTileC = 128;                         // centroids per tile
+constexpr int kScK = 64;                              // K per stage
+constexpr int kScMaxN = 256;                          // hidden rows per CTA (MMA N)
+constexpr int kScMaxSplit = 8;                        // K parts at most
+constexpr uint32_t kScABytes = kScTileC * kScK * 2;  // 16 KB of centroids per stage
+
+struct ScoreParams {
+  CUtensorMap tmC;  // centroids [n_clusters, H] bf16, box 64 x 128
+  CUtensorMap tmH;  // hidden [R, H] bf16, box 64 x N
+  float* scores;    // [ksplit, R, n_clusters]
+  int* status;
+  int R, H, n_clusters, N, ksplit, kper;
+};
+
+__host__ __device__ inline uint32_t sc_stage_bytes(int N) { return kScABytes + static_cast<uint32_t>(N) * 128u; }
+__host__ __device__ inline uint32_t sc_tmem_cols(int N) { return N <= 32 ? 32u : (N <= 64 ? 64u : (N <= 128 ? 128u : 256u)); }
+
+__global__ void __launch_bounds__(kScThreads) cluster_score_tc_kernel(const __grid_constant__ ScoreParams p) {
+  extern __shared__ __align__(1024) uint8_t sc_raw[];
+  uint8_t* smem = sc_raw + ((1024u - (smem_u32(sc_raw) & 1023u)) & 1023u);
+  __shared__ __align__(8) uint64_t full[kScStages], empty[kScStages], done;
+  __shared__ uint32_t tmem_base;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tile = blockIdx.x / p.ksplit, part = blockIdx.x - tile * p.ksplit;
+  const int ksteps = p.H / kScK;
+  const int k0 = part * p.kper, nk = max(0, min(ksteps, k0 + p.kper) - k0);
+  const uint32_t sbytes = sc_stage_bytes(p.N), ncols = sc_tmem_cols(p.N);
+  grid_dep_launch();
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kScStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(&done, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(&tmem_base, ncols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base;
+  // the hidden rows may come from the previous kernel, and the previous call's
+  // selection still reads the scores
+  grid_dep_wait();
+  if (warp == 0 && lane == 0) {
+    int i = 0;
+    for (; i < nk; ++i) {
+      const int s = i % kScStages;
+      if (i >= kScStages && !mbar_wait(&empty[s], ((i / kScStages) - 1) & 1, p.status, kWaitLimitCycles)) break;
+      uint8_t* a = smem + s * sbytes;
+      mbar_arrive_expect_tx(&full[s], sbytes);
+      tma_load_2d(a, &p.tmC, (k0 + i) * kScK, tile * kScTileC, &full[s]);
+      tma_load_2d(a + kScABytes, &p.tmH, (k0 + i) * kScK, static_cast<int>(blockIdx.y) * p.N, &full[s]);
+    }
+    // the copies of the last stages land before the CTA exits
+    for (int j = (i > kScStages ? i - kScStages : 0); j < i; ++j)
+      mbar_wait(&full[j % kScStages], (j / kScStages) & 1, p.status, kWaitLimitCycles);
+  } else if (warp == 1 && lane == 0) {
+    const uint32_t idesc = idesc_bf16_f32(kScTileC, p.N);
+    bool ok = nk > 0;
+    for (int i = 0; i < nk; ++i) {
+      const int s = i % kScStages;
+      if (!mbar_wait(&full[s], (i / kScStages) & 1, p.status, kWaitLimitCycles)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint64_t ad = smem_desc_k128(smem_u32(smem + s * sbytes));
+      const uint64_t bd = smem_desc_k128(smem_u32(smem + s * sbytes + kScABytes));
+#pragma unroll
+      for (int kk = 0; kk < kScK / 16; ++kk) tc_mma(tmem, ad + 2 * kk, bd + 2 * kk, idesc, i > 0 || kk > 0);
+      tc_commit(&empty[s]);  // the stage is free once these MMAs have read it
+    }
+    if (ok)
+      tc_commit(&done);
+    else
+      mbar_arrive(&done);  // status already set (or no K step): the epilogue stores nothing
+  }
+  __syncwarp();
+  const bool got = mbar_wait(&done, 0, p.status, kWaitLimitCycles) && nk > 0;
+  tc_fence_after();
+  const int c = tile * kScTileC + warp * 32 + lane;
+  const int r0 = static_cast<int>(blockIdx.y) * p.N;
+  float* out = p.scores + static_cast<size_t>(part) * p.R * p.n_clusters;
+  for (int g = 0; g < p.N; g += 32) {
+    float v[32];
+    tmem_ld32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + static_cast<uint32_t>(g), v);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const int r = r0 + g + j;
+      if (got && g + j < p.N && r < p.R && c < p.n_clusters) out[static_cast<size_t>(r) * p.n_clusters + c] = v[j];
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, ncols);
 }
 
 // Block-wide exclusive scan of one int per thread (all threads call); also
@@ -156,8 +276,30 @@ __global__ void __launch_bounds__(kHeadThreads, 1) cluster_topk_kernel(const __g
   grid_dep_wait();
   const int r = blockIdx.x, t = threadIdx.x;
   const int Nc = p.n_clusters;
+  // the K parts of the score GEMM, added in order; a thread's loads (four
+  // clusters x every part) are all issued before the first add
   const float* z = p.scores + static_cast<size_t>(r) * Nc;
-  for (int c = t; c < Nc; c += kHeadThreads) keys[c] = logit_key(z[c]);
+  const size_t part_stride = static_cast<size_t>(p.R) * Nc;
+  constexpr int kCPer = 4;
+  for (int c0 = t; c0 < Nc; c0 += kHeadThreads * kCPer) {
+    float part[kCPer][kScMaxSplit];
+#pragma unroll
+    for (int i = 0; i < kCPer; ++i) {
+      const int c = c0 + i * kHeadThreads;
+#pragma unroll
+      for (int q = 0; q < kScMaxSplit; ++q)
+        part[i][q] = (c < Nc && q < p.ksplit) ? __ldcg(z + q * part_stride + c) : 0.f;
+    }
+#pragma unroll
+    for (int i = 0; i < kCPer; ++i) {
+      const int c = c0 + i * kHeadThreads;
+      float zc = part[i][0];
+#pragma unroll
+      for (int q = 1; q < kScMaxSplit; ++q)
+        if (q < p.ksplit) zc += part[i][q];
+      if (c < Nc) keys[c] = logit_key(zc);
+    }
+  }
   __syncthreads();
   int greater;
   const uint32_t prefix = tk_block_kth(keys, Nc, p.top_k, hist, s_val, &greater);

@@ -77,7 +77,9 @@ int device_info(DeviceInfo* out) {
     if (cudaFuncSetAttribute(cluster_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kHeadMaxClusters * 4) != cudaSuccess ||
         cudaFuncSetAttribute(cand_sort_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kHeadSortSmemBitmap)) != cudaSuccess)
+                             static_cast<int>(kHeadSortSmemBitmap)) != cudaSuccess ||
+        cudaFuncSetAttribute(cluster_score_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kScStages * sc_stage_bytes(kScMaxN) + 1024)) != cudaSuccess)
       return SPEC_ERR_CUDA;
     const char* env = std::getenv("SPECV_ROW_LOADS");
     d.path = (env != nullptr && std::strcmp(env, "tma") == 0) ? kTma : kLdg;
@@ -595,13 +597,24 @@ struct HeadLayout {
   size_t header, scores, sel, pos, total;
 };
 
+// Shape of the cluster-score GEMM for R hidden rows: row chunks of N (a
+// multiple of 16, at most 256), and at most sc_max_split(R, n_clusters) K
+// parts: split K only while there are few tiles (a few dozen CTAs at most
+// otherwise), which also bounds the partial-score workspace.
+int sc_rows_n(int R) { return R >= kScMaxN ? kScMaxN : ((R + 15) / 16) * 16; }
+int sc_max_split(int R, int n_clusters) {
+  const long long tiles = (n_clusters + kScTileC - 1) / kScTileC;
+  const long long chunks = (R + sc_rows_n(R) - 1) / sc_rows_n(R);
+  return tiles * chunks <= 64 ? kScMaxSplit : 1;
+}
+
 HeadLayout head_layout(int R, int n_clusters, int top_k) {
   HeadLayout L;
   size_t off = 0;
   L.header = off;
   off += align_up(sizeof(WsHeader), 256);
-  L.scores = off;
-  off += align_up(static_cast<size_t>(R) * n_clusters * sizeof(float), 256);
+  L.scores = off;  // the K parts' partial scores
+  off += align_up(static_cast<size_t>(sc_max_split(R, n_clusters)) * R * n_clusters * sizeof(float), 256);
   L.sel = off;
   off += align_up(static_cast<size_t>(R) * top_k * sizeof(int32_t), 256);
   L.pos = off;
@@ -1003,11 +1016,40 @@ int spec_centroid_head(const void* hidden, const void* centroids, const void* W_
   hp.top_k = top_k;
   hp.max_cand = max_cand;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const dim3 g1((n_clusters + kHeadWarps - 1) / kHeadWarps, (R + kHeadRowBlock - 1) / kHeadRowBlock);
+  // the score GEMM (more than kHeadScoreTcRows rows): 128-centroid tiles x
+  // row chunks, K split so that the grid has about two CTAs per SM
+  const bool sc_tc = R > kHeadScoreTcRows;
+  ScoreParams sp;
+  std::memset(&sp, 0, sizeof(sp));
+  sp.N = sc_rows_n(R);
+  if (sc_tc && (!encode_rows(&sp.tmC, centroids, n_clusters, H, kScTileC) ||
+                !encode_rows(&sp.tmH, hidden, R, H, sp.N)))
+    return SPEC_ERR_CUDA;
+  const int tiles = (n_clusters + kScTileC - 1) / kScTileC, chunks = (R + sp.N - 1) / sp.N;
+  const int ksteps = H / kScK;
+  int ksplit = (2 * dev.sms + tiles * chunks - 1) / (tiles * chunks);
+  const int max_split = sc_max_split(R, n_clusters);
+  if (ksplit > max_split) ksplit = max_split;
+  if (ksplit > ksteps) ksplit = ksteps;
+  if (ksplit < 1) ksplit = 1;
+  sp.kper = (ksteps + ksplit - 1) / ksplit;
+  sp.ksplit = (ksteps + sp.kper - 1) / sp.kper;  // no empty part
+  sp.scores = hp.scores;
+  sp.status = hp.status;
+  sp.R = R;
+  sp.H = H;
+  sp.n_clusters = n_clusters;
+  hp.ksplit = sc_tc ? sp.ksplit : 1;
+  const size_t sc_smem = static_cast<size_t>(kScStages) * sc_stage_bytes(sp.N) + 1024;
   const size_t sort1 = static_cast<size_t>(n_clusters) * sizeof(uint32_t);
   const size_t sort2 = (V <= kHeadBitmapV) ? kHeadSortSmemBitmap
                                            : static_cast<size_t>(pow2_at_least(max_cand)) * sizeof(unsigned long long);
-  if (launch_pdl(cluster_score_kernel, g1, dim3(kHeadThreads), 0, st, hp) != cudaSuccess ||
+  const cudaError_t e_sc =
+      sc_tc ? launch_pdl(cluster_score_tc_kernel, dim3(tiles * sp.ksplit, chunks), dim3(kScThreads), sc_smem, st, sp)
+            : launch_pdl(cluster_score_cc_kernel,
+                         dim3((n_clusters + kHeadWarps - 1) / kHeadWarps, (R + kHeadRowBlock - 1) / kHeadRowBlock),
+                         dim3(kHeadThreads), 0, st, hp);
+  if (e_sc != cudaSuccess ||
       launch_pdl(cluster_topk_kernel, dim3(R), dim3(kHeadThreads), sort1, st, hp) != cudaSuccess ||
       launch_pdl(cand_logit_kernel, dim3(top_k, R), dim3(kHeadThreads), 0, st, hp) != cudaSuccess ||
       launch_pdl(cand_sort_kernel, dim3(R), dim3(kHeadThreads), sort2, st, hp) != cudaSuccess)

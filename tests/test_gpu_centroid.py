@@ -69,6 +69,27 @@ def test_head_exact_small(sv):
             assert np.array_equal(lg[r, :cnt[r]].astype(np.float64), l_ref)  # exact recipe: bitwise
 
 
+@pytest.mark.parametrize("B,gamma,n_clusters,H,top_k", [
+    (12, 3, 200, 512, 24),   # R = 36: one row chunk of 48, a ragged last 128-cluster tile
+    (100, 3, 256, 256, 16),  # R = 300: two row chunks (256 + 44), four K steps
+])
+def test_head_exact_tensor_core_scores(sv, B, gamma, n_clusters, H, top_k):
+    """More than 16 hidden rows: the cluster scores come from the tcgen05
+    GEMM with K split over several CTAs; on the exact-sums recipe the
+    selection, the candidates and their logits equal the oracle bitwise."""
+    m = wl.make_centroid_model(V=16384, H=H, n_clusters=n_clusters, seed=9, exact_sums=True, mu_sd=0.12,
+                               eps_sd=0.005)
+    rd = wl.make_centroid_round(m, B=B, gamma=gamma, exact_sums=True, draft_sd=0.05)
+    assert rd["hidden_draft"].shape[0] == B * gamma > 16
+    tok, lg, cnt, st = _run_head(sv, m, rd["hidden_draft"], top_k)
+    assert st == sv.SPEC_OK
+    ref = oracle.centroid_head(rd["hidden_draft"], m.centroids, m.W_ord, m.cluster_off, m.ord2tok, top_k)
+    for r, (t_ref, l_ref) in enumerate(ref):
+        assert cnt[r] == len(t_ref), r
+        assert np.array_equal(tok[r, :cnt[r]], t_ref), r
+        assert np.array_equal(lg[r, :cnt[r]].astype(np.float64), l_ref), r
+
+
 def test_head_exact_past_the_bitmap_vocabulary(sv):
     """Above 262,144 tokens the candidates are ordered by the sort kernel (a
     bitonic sort) instead of the selection kernel's ranks; same bar: bitwise."""
