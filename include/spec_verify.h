@@ -206,8 +206,9 @@ int spec_verify_sample_topkp(const void *target_logits, const void *draft_logits
  * clusters hold more than max_cand tokens keeps the first max_cand (in
  * cluster-score order) and makes spec_verify_status return
  * SPEC_ERR_UNSUPPORTED.  The workspace (spec_centroid_head_workspace_bytes,
- * zeroed once by spec_verify_workspace_init) holds the scores, the selection
- * and the status word.  Asynchronous; host checks return negative codes.
+ * zeroed once by spec_verify_workspace_init) holds the scores (up to 8
+ * partial sums per score while R x n_clusters is small: the score GEMM's K
+ * parts), the selection and the status word.  Asynchronous; host checks return negative codes.
  */
 int spec_centroid_head_workspace_bytes(int R, int n_clusters, int top_k, size_t *bytes);
 
