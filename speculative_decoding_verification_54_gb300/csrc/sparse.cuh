@@ -32,6 +32,7 @@ namespace specv {
 constexpr int kSparseThreads = 512;
 constexpr int kSparseWarps = kSparseThreads / 32;
 constexpr int kSparseStage = 2048;  // candidates of a CTA's chunk range staged in shared memory
+constexpr int kSparseRowStage = 4096;  // a row's candidate tokens staged whole (the draw's mass buffer)
 
 struct SparseParams {
   const void* target;          // [B, gamma+1, V]
@@ -340,30 +341,55 @@ __global__ void __launch_bounds__(kSparseThreads, 1) sparse_tail_kernel(const __
 
   if (s.mode == kModeResidual) {
     const int ncand = cand_n(p, drow);
-    // ---- this CTA's candidates, staged with their q ----
-    if (warp == 0) {
-      const int lo = warp_lower_bound(GlobalI32{tok}, ncand, c0 * p.CE);
-      if (lane == 0) s_lo = lo;
-    } else if (warp == 1) {
-      const int hi = warp_lower_bound(GlobalI32{tok}, ncand, c1 * p.CE);
-      if (lane == 0) s_hi = hi;
-    }
-    __syncthreads();
-    const int lo = s_lo, nst = s_hi - s_lo;
-    const bool staged = nst <= kSparseStage;
-    if (staged) {
-      for (int i = threadIdx.x; i < nst; i += kSparseThreads) {
-        st_tok[i] = __ldg(tok + lo + i);
-        st_q[i] = f.q(__ldg(lg + lo + i));
+    // ---- the candidates: the whole row's tokens in shared memory when they
+    // fit (the draw's mass buffer, free until then: one load round, and every
+    // search after it is in shared memory; the q values are loaded with the
+    // chunk's logits); otherwise this CTA's share, found by searches in
+    // global memory and staged with its q ----
+    int32_t* rowtok = reinterpret_cast<int32_t*>(sm_mass);
+    const bool whole = ncand <= kSparseRowStage;
+    int lo = 0, nst = ncand;
+    bool staged = true;
+    if (whole) {
+      constexpr int kPer = kSparseRowStage / kSparseThreads;
+      int32_t tv[kPer];
+#pragma unroll
+      for (int j = 0; j < kPer; ++j) {
+        const int i = static_cast<int>(threadIdx.x) + j * kSparseThreads;
+        tv[j] = (i < ncand) ? __ldg(tok + i) : 0;
+      }
+#pragma unroll
+      for (int j = 0; j < kPer; ++j) {
+        const int i = static_cast<int>(threadIdx.x) + j * kSparseThreads;
+        if (i < ncand) rowtok[i] = tv[j];
+      }
+    } else {
+      if (warp == 0) {
+        const int l = warp_lower_bound(GlobalI32{tok}, ncand, c0 * p.CE);
+        if (lane == 0) s_lo = l;
+      } else if (warp == 1) {
+        const int h = warp_lower_bound(GlobalI32{tok}, ncand, c1 * p.CE);
+        if (lane == 0) s_hi = h;
+      }
+      __syncthreads();
+      lo = s_lo;
+      nst = s_hi - s_lo;
+      staged = nst <= kSparseStage;
+      if (staged) {
+        for (int i = threadIdx.x; i < nst; i += kSparseThreads) {
+          st_tok[i] = __ldg(tok + lo + i);
+          st_q[i] = f.q(__ldg(lg + lo + i));
+        }
       }
     }
     __syncthreads();
+    const int32_t* stok = whole ? rowtok : st_tok;  // staged tokens, from index lo
     // ---- chunk masses: one warp per chunk ----
     for (int c = c0 + warp; c < c1; c += kSparseWarps) {
       int a, e;
       if (staged) {
-        a = warp_lower_bound(SmemI32{st_tok}, nst, c * p.CE);
-        e = warp_lower_bound(SmemI32{st_tok}, nst, (c + 1) * p.CE);
+        a = warp_lower_bound(SmemI32{stok}, nst, c * p.CE);
+        e = warp_lower_bound(SmemI32{stok}, nst, (c + 1) * p.CE);
       } else {
         a = warp_lower_bound(GlobalI32{tok + lo}, nst, c * p.CE);
         e = warp_lower_bound(GlobalI32{tok + lo}, nst, (c + 1) * p.CE);
@@ -383,8 +409,8 @@ __global__ void __launch_bounds__(kSparseThreads, 1) sparse_tail_kernel(const __
       int x0 = -1;
       float xp0 = 0.f, q0 = 0.f;
       if (a + lane < e) {
-        x0 = staged ? st_tok[a + lane] : __ldg(tok + lo + a + lane);
-        q0 = staged ? st_q[a + lane] : f.q(__ldg(lg + lo + a + lane));
+        x0 = staged ? stok[a + lane] : __ldg(tok + lo + a + lane);
+        q0 = (staged && !whole) ? st_q[a + lane] : f.q(__ldg(lg + lo + a + lane));
         if (x0 >= 0 && x0 < p.V) xp0 = load_logit<T>(p.target, rowp_n * p.V + x0);
       }
       // compensated (Neumaier) sums per lane, four independent chains;
@@ -404,9 +430,9 @@ __global__ void __launch_bounds__(kSparseThreads, 1) sparse_tail_kernel(const __
       float s1 = 0.f, c1m = 0.f;
       if (x0 >= 0 && x0 < p.V) neumaier_add(s1, c1m, fminf(f.p(xp0), q0));
       for (int i = a + lane + 32; i < e; i += 32) {
-        const int x = staged ? st_tok[i] : __ldg(tok + lo + i);
+        const int x = staged ? stok[i] : __ldg(tok + lo + i);
         if (x < 0 || x >= p.V) continue;  // not a token: no weight to take off
-        const float q = staged ? st_q[i] : f.q(__ldg(lg + lo + i));
+        const float q = (staged && !whole) ? st_q[i] : f.q(__ldg(lg + lo + i));
         const float pp = f.p(load_logit<T>(p.target, rowp_n * p.V + x));
         neumaier_add(s1, c1m, fminf(pp, q));
       }
