@@ -121,11 +121,97 @@ __device__ __forceinline__ float dot_row(const uint4* h4, const uint4* w4, int n
   return warp_sum(acc0 + acc1);
 }
 
+// Level 1 of the inverse-CDF draw over tile masses staged in shared memory,
+// by the whole CTA (every thread calls; a warp alone walked 2,048 masses 64
+// per lane, about 6 K cycles): thread t owns the contiguous tiles
+// [t*per, (t+1)*per), and a block scan of the two-float range sums gives each
+// thread its inclusive prefix and every thread the total Z.
+struct BlockMassScan {
+  F2 lsum, incl, Z;
+  int c0, c1;
+};
+__device__ __forceinline__ BlockMassScan block_scan_masses(const float* sm, int n, F2* s_w) {
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const int per = (n + kLmTailThreads - 1) / kLmTailThreads;
+  BlockMassScan bs;
+  bs.c0 = min(n, t * per);
+  bs.c1 = min(n, bs.c0 + per);
+  bs.lsum = f2_from(0.f);
+  for (int c = bs.c0; c < bs.c1; ++c) bs.lsum = f2_add(bs.lsum, f2_from(sm[c]));
+  const F2 wincl = warp_scan_incl(bs.lsum);
+  if (lane == 31) s_w[warp] = wincl;
+  __syncthreads();
+  F2 before = f2_from(0.f), Z = f2_from(0.f);
+  for (int w = 0; w < kLmTailWarps; ++w) {
+    const F2 x = s_w[w];
+    if (w < warp) before = f2_add(before, x);
+    Z = f2_add(Z, x);
+  }
+  __syncthreads();  // s_w free again
+  bs.incl = f2_add(before, wincl);
+  bs.Z = Z;
+  return bs;
+}
+
+// The tile holding `target` (= u*Z), as pick_chunk_fn, by the whole CTA: the
+// first thread whose inclusive prefix exceeds the target walks its tiles.
+// *local: target minus the mass before that tile, or FLT_MAX when rounding
+// puts the target at or beyond the total (then the last tile of nonzero mass).
+__device__ __forceinline__ int block_pick_tile(const float* sm, const BlockMassScan& bs, F2 target, F2* local,
+                                               int* s_i, F2* s_loc) {
+  const int t = threadIdx.x;
+  if (t == 0) {
+    s_i[0] = INT_MAX;
+    s_i[1] = -1;
+  }
+  __syncthreads();
+  if (f2_gt(bs.incl, target)) atomicMin(&s_i[0], t);
+  __syncthreads();
+  const int L = s_i[0];
+  if (t == L) {
+    int tile = -1;
+    F2 loc = F2{FLT_MAX, 0.f};
+    F2 run = f2_sub(bs.incl, bs.lsum);
+    for (int c = bs.c0; c < bs.c1; ++c) {
+      const F2 nxt = f2_add(run, f2_from(sm[c]));
+      if (f2_gt(nxt, target)) {
+        tile = c;
+        loc = f2_sub(target, run);
+        break;
+      }
+      run = nxt;
+    }
+    if (tile < 0)  // rounding inside the range: its last nonzero tile
+      for (int c = bs.c1 - 1; c >= bs.c0; --c)
+        if (sm[c] > 0.f) {
+          tile = c;
+          break;
+        }
+    s_i[1] = tile;
+    *s_loc = loc;
+  }
+  if (L == INT_MAX) {  // u*Z at or beyond the total: the last nonzero tile
+    int last = -1;
+    for (int c = bs.c0; c < bs.c1; ++c)
+      if (sm[c] > 0.f) last = c;
+    if (last >= 0) atomicMax(&s_i[1], last);
+    if (t == 0) *s_loc = F2{FLT_MAX, 0.f};
+  }
+  __syncthreads();
+  const int tile = s_i[1];
+  *local = *s_loc;
+  __syncthreads();  // s_i, s_loc free again
+  return tile < 0 ? 0 : tile;
+}
+
 __global__ void __launch_bounds__(kLmTailThreads) lm_tail_kernel(const __grid_constant__ LmTailParams p) {
   __shared__ float xs[kLmTileV];
   __shared__ float sm_mass[kLmSmemTiles];
   __shared__ int s_last, s_chunk, s_plain;
   __shared__ F2 s_local;
+  __shared__ F2 s_w[kLmTailWarps];
+  __shared__ int s_pi[2];
+  __shared__ F2 s_ploc;
   const int b = blockIdx.y, part = blockIdx.x;
   const bool staged = p.n_tiles <= kLmSmemTiles;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -175,18 +261,18 @@ __global__ void __launch_bounds__(kLmTailThreads) lm_tail_kernel(const __grid_co
     if (staged) {
       for (int c = threadIdx.x; c < p.n_tiles; c += kLmTailThreads) sm_mass[c] = pm(c);
       __syncthreads();
-    }
-    if (warp == 0) {
+      const BlockMassScan bs = block_scan_masses(sm_mass, p.n_tiles, s_w);
       F2 local;
-      int chunk;
-      if (staged) {
-        const SmemMass sm{sm_mass};
-        const MassScan ms = scan_masses_fn(sm, p.n_tiles);
-        chunk = pick_chunk_fn(sm, ms, f2_mul_f(ms.Z, p.u_resample[b]), &local);
-      } else {
-        const MassScan ms = scan_masses_fn(pm, p.n_tiles);
-        chunk = pick_chunk_fn(pm, ms, f2_mul_f(ms.Z, p.u_resample[b]), &local);
+      const int chunk = block_pick_tile(sm_mass, bs, f2_mul_f(bs.Z, p.u_resample[b]), &local, s_pi, &s_ploc);
+      if (threadIdx.x == 0) {
+        s_chunk = chunk;
+        s_local = local;
+        s_plain = 1;
       }
+    } else if (warp == 0) {
+      F2 local;
+      const MassScan ms = scan_masses_fn(pm, p.n_tiles);
+      const int chunk = pick_chunk_fn(pm, ms, f2_mul_f(ms.Z, p.u_resample[b]), &local);
       if (lane == 0) {
         s_chunk = chunk;
         s_local = local;
@@ -218,25 +304,22 @@ __global__ void __launch_bounds__(kLmTailThreads) lm_tail_kernel(const __grid_co
   if (residual && staged) {  // level 1 over the residual tile masses, staged in shared memory
     for (int c = threadIdx.x; c < p.n_tiles; c += kLmTailThreads) sm_mass[c] = __ldcg(mass + c);
     __syncthreads();
-    if (warp == 0) {
-      const SmemMass sm{sm_mass};
-      MassScan ms = scan_masses_fn(sm, p.n_tiles);
-      const bool z0 = !(ms.Z.hi > 0.f);
-      if (z0) {
-        // Z == 0 cannot happen in exact arithmetic; if rounding produces it,
-        // draw from p_n itself (tile masses from its partials)
-        const PartialMass pn{p.tpart + static_cast<size_t>(b * (g + 1) + s.n) * p.n_tiles, rp.mk};
-        for (int c = lane; c < p.n_tiles; c += 32) sm_mass[c] = pn(c);
-        __syncwarp();
-        ms = scan_masses_fn(sm, p.n_tiles);
-      }
-      F2 local;
-      const int chunk = pick_chunk_fn(sm, ms, f2_mul_f(ms.Z, p.u_resample[b]), &local);
-      if (lane == 0) {
-        s_chunk = chunk;
-        s_local = local;
-        s_plain = z0;
-      }
+    BlockMassScan bs = block_scan_masses(sm_mass, p.n_tiles, s_w);
+    const bool z0 = !(bs.Z.hi > 0.f);  // uniform over the CTA
+    if (z0) {
+      // Z == 0 cannot happen in exact arithmetic; if rounding produces it,
+      // draw from p_n itself (tile masses from its partials)
+      const PartialMass pn{p.tpart + static_cast<size_t>(b * (g + 1) + s.n) * p.n_tiles, rp.mk};
+      for (int c = threadIdx.x; c < p.n_tiles; c += kLmTailThreads) sm_mass[c] = pn(c);
+      __syncthreads();
+      bs = block_scan_masses(sm_mass, p.n_tiles, s_w);
+    }
+    F2 local;
+    const int chunk = block_pick_tile(sm_mass, bs, f2_mul_f(bs.Z, p.u_resample[b]), &local, s_pi, &s_ploc);
+    if (threadIdx.x == 0) {
+      s_chunk = chunk;
+      s_local = local;
+      s_plain = z0;
     }
   } else if (residual && warp == 0) {  // level 1 over the residual tile masses in global memory
     bool plain = false;
