@@ -165,8 +165,9 @@ struct LmEpiScratch {
 // Phase 1: per 32-row group, the warp's column maxima (and argmax where a row
 // is greedy) into red/redI.  Phase 2: lane l combines the four quadrants for
 // row l of each group.  Phase 3: exponentials against the row maxima, the
-// stored logits, and the warp's column sums into red; this group's reads of
-// the TMEM chunk end with this phase.  Phase 4: the row partials.  The group
+// stored logits, and the warp's column sums into red; each warp frees the
+// TMEM slot right after its last read of the chunk.  Phase 4: the row
+// partials.  The group
 // loops stay rolled (the unrolled bodies overflow the instruction cache);
 // what crosses phases lives in shared memory.
 __device__ __forceinline__ void lm_epilogue_chunk(const LmParams& p, const LmRowTables& T, const LmEpiScratch& S,
@@ -233,10 +234,23 @@ __device__ __forceinline__ void lm_epilogue_chunk(const LmParams& p, const LmRow
   named_bar(bar_id, 128);
 
   // ---- phase 3 ----
+  // The slot is released right after this warp's last TMEM read of the
+  // chunk (the values are in registers from then on), so the next tile's
+  // MMAs do not wait for the last group's exponentials and stores.
+  if (g0 >= ng) {  // no 32-row group of this chunk for this group
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(slot_empty);
+  }
 #pragma unroll 1
   for (int g = g0; g < ng; g += 2) {
     float v[32];
     tmem_ld32(tacc + g * 32, v);
+    if (g + 2 >= ng) {  // this warp's last read of the chunk
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(slot_empty);
+    }
     const int rb = c * nc + g * 32;
     const bool anys = __any_sync(0xffffffffu, S.fin[g * 32 + lane].y < INFINITY);
     const int srl = (rb + lane < p.R) ? T.srow[rb + lane] : -1;
@@ -275,9 +289,6 @@ __device__ __forceinline__ void lm_epilogue_chunk(const LmParams& p, const LmRow
       S.red[quad * nc + g * 32 + lane] = v[0];
     }
   }
-  tc_fence_before();
-  __syncwarp();
-  if (lane == 0) mbar_arrive(slot_empty);  // this warp's reads of the chunk are done
   named_bar(bar_id, 128);
 
   // ---- phase 4 ----
