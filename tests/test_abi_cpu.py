@@ -308,6 +308,16 @@ def test_centroid_and_sparse_workspace_bytes(lib):
     assert lib.spec_centroid_head_workspace_bytes(4, 2048, 32, ctypes.byref(out)) == sv.SPEC_OK
     assert out.value >= 4 * 2048 * 4 + 4 * 32 * 4 + 4 * 33 * 4
     assert lib.spec_centroid_head_workspace_bytes(4, 2048, 3000, ctypes.byref(out)) == sv.SPEC_ERR_INVALID_ARG
+    # the score GEMM's K parts: while tiles (128 clusters) x row chunks (256
+    # rows) are few, up to 8 partial sums per score; otherwise one
+    def head_ws(R, nc):
+        assert lib.spec_centroid_head_workspace_bytes(R, nc, 8, ctypes.byref(out)) == sv.SPEC_OK
+        return out.value
+    small = head_ws(128, 2048)           # 16 tiles x 1 chunk: split
+    assert small >= 8 * 128 * 2048 * 4
+    large = head_ws(64 * 256, 2048)      # 16 tiles x 64 chunks: no split
+    assert 64 * 256 * 2048 * 4 <= large < 2 * 64 * 256 * 2048 * 4
+    assert head_ws(4, 2048) >= 8 * 4 * 2048 * 4
     plain = sv.spec_verify_workspace_bytes(32, 4, 262144)
     assert lib.spec_verify_sparse_workspace_bytes(32, 4, 262144, ctypes.byref(out)) == sv.SPEC_OK
     assert out.value >= plain + 32 * 257 * 4     # per-chunk candidate offsets
