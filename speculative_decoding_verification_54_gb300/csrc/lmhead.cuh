@@ -19,10 +19,13 @@
 //   warp 2     one thread issues tcgen05.mma (M=128, N=chunk, K=16) and
 //              commits each stage back to its ring, and each finished chunk to
 //              the epilogue;
-//   warps 3-10 two groups of four (one warp per TMEM lane quadrant) take
-//              alternate accumulator chunks.  The accumulator rotates through
+//   warps 3-10 two groups of four (one warp per TMEM lane quadrant); both
+//              work on every accumulator chunk, group g on its 32-row groups
+//              of parity g, and each warp frees the chunk's TMEM slot right
+//              after its last read of it.  The accumulator rotates through
 //              512/chunk TMEM slots, so the epilogue of one chunk overlaps the
-//              MMAs of the next;
+//              MMAs of the next (the next tile's second chunk reuses the slot
+//              of this tile's first);
 //   warps 11-14 the row reducer's work for the draft rows (their chunk
 //              statistics), streamed from HBM beside the GEMM, which leaves
 //              most of the HBM bandwidth idle.
