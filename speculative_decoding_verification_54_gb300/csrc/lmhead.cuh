@@ -57,7 +57,10 @@ constexpr int kLmMaxRows = 384;     // hidden rows per call
 constexpr int kLmMaxChunk = 256;    // MMA N limit
 constexpr uint32_t kLmWBytes = kLmTileV * kLmTileK * 2;  // 16 KB
 constexpr int kLmMaxWStages = 6, kLmMaxHStages = 6, kLmMaxSlots = 4;
-constexpr int kLmWPrefetch = 12;  // W steps prefetched into L2 ahead of the ring (192 KB per CTA)
+// W steps prefetched into L2 ahead of the ring (64 KB per CTA).  Measured (GEMM
+// alone, B=64, H=1536, one box): 4 steps 241.6 us, 8 steps 244.0, 12 steps
+// 245.7, 20 steps 276.2, 32 steps 300.6: a long lead only evicts lines.
+constexpr int kLmWPrefetch = 4;
 constexpr int kLmEpiGroups = 2;                                         // of four warps
 constexpr int kLmRowWarp0 = 3 + 4 * kLmEpiGroups;                       // first row warp
 constexpr int kLmRowWarps = 4;                                          // the draft rows' statistics
